@@ -1,0 +1,174 @@
+"""Golden / reference / target correctness gate.
+
+TEST INFRASTRUCTURE: see the package docstring.
+
+Follows the page "torchtitan kernel numerics verification" (sections on the three
+implementations, the correctness gate, the conditioning check, the per-element
+condition number of reductions and the report table):
+
+  1. Structure first: shapes equal, then the positions of NaN, +Inf and -Inf in
+     the target (and in the reference) equal those of the golden result as the
+     output dtype holds it.
+  2. In fp64:
+        reference_error = max |reference - golden|
+        target_error    = max |target - golden|
+        rounding_floor  = max |golden.to(out_dtype).to(fp64) - golden|
+        absolute_floor  = max(PROJECT_ATOL, rounding_floor)
+        threshold       = FUDGE_FACTOR * reference_error + absolute_floor
+  3. Conditioning: reference_error / max(max|golden|, absolute_floor) must not
+     exceed MAX_REFERENCE_RELATIVE_ERROR, else no PASS/FAIL verdict is given
+     (INCONCLUSIVE: "reference is too inaccurate to gate the target").
+  4. PASS iff target_error <= threshold.
+
+The constants are declared here, before any target runs, and are never changed
+to make a failing target pass.  For float32 I/O an additional normwise bound
+max|target - golden| / max|golden| <= FP32_MAX_RELATIVE_ERROR applies.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import oracle
+
+FUDGE_FACTOR = 2.0
+PROJECT_ATOL = 0.0
+MAX_REFERENCE_RELATIVE_ERROR = 0.1
+FP32_MAX_RELATIVE_ERROR = 1e-5
+
+
+@dataclass
+class GateResult:
+    tensor: str
+    dtype: str
+    reference_error: float = float("nan")
+    target_error: float = float("nan")
+    rounding_floor: float = float("nan")
+    absolute_floor: float = float("nan")
+    threshold: float = float("nan")
+    golden_scale: float = float("nan")
+    reference_relative_error: float = float("nan")
+    condition: float | None = None
+    gate_valid: bool = False
+    verdict: str = "FAIL"
+    notes: list = field(default_factory=list)
+
+    @property
+    def passed(self) -> bool:
+        return self.verdict == "PASS"
+
+    def row(self) -> str:
+        cond = "-" if self.condition is None else f"{self.condition:.3g}"
+        return (f"| {self.tensor} | {self.reference_error:.3e} ({self.reference_relative_error:.2e} rel) "
+                f"| {cond} | {self.target_error:.3e} | {self.threshold:.3e} "
+                f"| {'yes' if self.gate_valid else 'no'} | {self.verdict} |")
+
+
+TABLE_HEADER = ("| Tensor | Ref/golden | Condition | Target err | Threshold | Gate valid | Verdict |\n"
+                "|---|---|---|---|---|---|---|")
+
+
+def _structure(golden_held: np.ndarray, other: np.ndarray) -> list:
+    problems = []
+    if np.any(np.isnan(golden_held) != np.isnan(other)):
+        problems.append("NaN positions differ")
+    if np.any(np.isposinf(golden_held) != np.isposinf(other)):
+        problems.append("+Inf positions differ")
+    if np.any(np.isneginf(golden_held) != np.isneginf(other)):
+        problems.append("-Inf positions differ")
+    return problems
+
+
+def check(tensor: str, golden: np.ndarray, reference: np.ndarray, target: np.ndarray,
+          out_dtype: str, rel_bound: float | None = None,
+          condition: float | None = None) -> GateResult:
+    """Apply the gate to one output or gradient tensor.
+
+    ``golden`` is fp64; ``reference`` and ``target`` are fp64 arrays holding the
+    exact values of the two low-precision results (decode them first).
+    ``out_dtype`` is the dtype the target stores the tensor in (it sets the
+    rounding floor). ``rel_bound`` adds the normwise relative bound.
+    """
+    res = GateResult(tensor=tensor, dtype=out_dtype, condition=condition)
+    golden = np.asarray(golden, np.float64)
+    reference = np.asarray(reference, np.float64)
+    target = np.asarray(target, np.float64)
+    if golden.shape != reference.shape or golden.shape != target.shape:
+        res.notes.append(f"shape mismatch {golden.shape} {reference.shape} {target.shape}")
+        return res
+    held = oracle.round_to(golden, out_dtype)
+    for who, arr in (("target", target), ("reference", reference)):
+        for p in _structure(held, arr):
+            res.notes.append(f"{who}: {p}")
+    if res.notes:
+        return res
+    finite = np.isfinite(held)
+    if finite.any():
+        g = golden[finite]
+        res.reference_error = float(np.max(np.abs(reference[finite] - g)))
+        res.target_error = float(np.max(np.abs(target[finite] - g)))
+        res.rounding_floor = float(np.max(np.abs(held[finite] - g)))
+        res.golden_scale = float(np.max(np.abs(g)))
+    else:
+        res.reference_error = res.target_error = res.rounding_floor = res.golden_scale = 0.0
+    res.absolute_floor = max(PROJECT_ATOL, res.rounding_floor)
+    res.threshold = FUDGE_FACTOR * res.reference_error + res.absolute_floor
+    denom = max(res.golden_scale, res.absolute_floor)
+    res.reference_relative_error = res.reference_error / denom if denom > 0 else 0.0
+    res.gate_valid = res.reference_relative_error <= MAX_REFERENCE_RELATIVE_ERROR
+    if not res.gate_valid:
+        res.verdict = "INCONCLUSIVE"
+        res.notes.append("reference is too inaccurate to gate the target")
+        return res
+    ok = res.target_error <= res.threshold
+    if not ok:
+        res.notes.append(f"target_error {res.target_error:.3e} > threshold {res.threshold:.3e}")
+    if rel_bound is not None and res.golden_scale > 0:
+        rel = res.target_error / res.golden_scale
+        if rel > rel_bound:
+            ok = False
+            res.notes.append(f"normwise relative error {rel:.3e} > {rel_bound:.1e}")
+    res.verdict = "PASS" if ok else "FAIL"
+    return res
+
+
+def overall(results) -> str:
+    verdicts = [r.verdict for r in results]
+    if any(v == "FAIL" for v in verdicts):
+        return "FAIL"
+    if any(v == "INCONCLUSIVE" for v in verdicts):
+        return "INCONCLUSIVE"
+    return "PASS"
+
+
+def report(title: str, results) -> str:
+    lines = [f"### {title}", TABLE_HEADER] + [r.row() for r in results]
+    for r in results:
+        for n in r.notes:
+            lines.append(f"- {r.tensor}: {n}")
+    lines.append(f"Overall: {overall(results)}")
+    return "\n".join(lines)
+
+
+# --------------------------------------------------------------------------- #
+# per-element condition numbers of the reductions (diagnostic column)
+# --------------------------------------------------------------------------- #
+def condition_number(terms: np.ndarray) -> float:
+    """sum|term| / |sum term| of one reduction, in fp64 (inf when the sum is 0)."""
+    terms = np.asarray(terms, np.float64)
+    s = abs(float(np.sum(terms)))
+    a = float(np.sum(np.abs(terms)))
+    return float("inf") if s == 0.0 else a / s
+
+
+def dgamma_condition(x: np.ndarray, dy: np.ndarray, rstd_golden: np.ndarray, col: int) -> float:
+    """Condition number of dgamma[col] = sum_i dy[i,col] * x[i,col] * r_i (fp64 inputs)."""
+    return condition_number(dy[:, col] * x[:, col] * rstd_golden)
+
+
+def worst_index(golden: np.ndarray, target: np.ndarray) -> int:
+    """Flat index of the element with the largest |target - golden| (finite only)."""
+    d = np.abs(np.asarray(target, np.float64) - np.asarray(golden, np.float64))
+    d[~np.isfinite(d)] = -1.0
+    return int(np.argmax(d))

@@ -1,0 +1,337 @@
+/*
+ * rmsnorm_oracle.c -- plain CPU oracle for row-wise RMSNorm, forward and backward.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+ * baseline use this file. The GPU library never links, includes or calls it, and
+ * it shares no code with the GPU library (its own dtype codes, its own number
+ * format conversions, its own loops).
+ *
+ * What it computes (page "Check an AI model calculation before accelerating it",
+ * sections "Problem and reference formula", "Why do we need a forward and a
+ * backward pass?", "Where does the cube of r come from?" and "A sum is not an
+ * average"), for a row-major M x N matrix x, a per-column weight gamma and an
+ * upstream gradient dy:
+ *
+ *     r      = 1 / sqrt(mean_j(x_j^2) + eps)          one number per row
+ *     y      = x * r * gamma                          elementwise
+ *     u      = dy * gamma
+ *     dx     = r * u - x * r^3 * mean_j(u_j * x_j)     mean over the N columns of a row
+ *     dgamma = sum over the M rows of dy * x * r       a sum, not a mean
+ *
+ * The offset variant (page "torchtitan kernel numerics verification", section on
+ * the golden / reference / target implementations) replaces gamma by (1 + w)
+ * wherever gamma appears; dgamma keeps the same formula because d(1+w)/dw = 1.
+ *
+ * Two arithmetic levels, following the three-implementation method of the
+ * torchtitan page:
+ *
+ *   golden     every input element is promoted exactly to fp64 and every step is
+ *              done in fp64; outputs stay fp64.
+ *   reference  every input element is converted to fp32 at load, every product,
+ *              sum, square root and division is an fp32 operation, sums run left
+ *              to right in index order, and each output (y, dx, dgamma) is rounded
+ *              once, to nearest-even, into the I/O dtype. rstd stays fp32.
+ *
+ * This file must be compiled with floating-point contraction disabled
+ * (-ffp-contract=off) so that every fp32 operation above is rounded on its own.
+ *
+ * Dtype codes used by this file: 0 = float32, 1 = float16, 2 = bfloat16.
+ * Element storage: float32 as IEEE binary32, float16 as IEEE binary16 bits,
+ * bfloat16 as the upper 16 bits of an IEEE binary32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+
+/* ------------------------------------------------------------------------- */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Exact value of an IEEE binary16 bit pattern. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = h >> 15;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);              /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x400), e - 25); /* (1024 + m) * 2^(e - 15 - 10) */
+    return sign ? -v : v;
+}
+
+/* Exact value of a bfloat16 bit pattern (the top half of a binary32). */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/*
+ * Round v to the nearest value of a binary floating-point format with `prec`
+ * significand bits (implicit bit included), smallest normal exponent `emin` and
+ * largest exponent `emax`; ties go to the even significand; values beyond the
+ * largest finite number become infinities (IEEE 754 round-to-nearest-even).
+ */
+static double round_to_format(double v, int prec, int emin, int emax) {
+    if (v != v || v == 0.0 || isinf(v)) return v;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);            /* a = f * 2^e with f in [0.5, 1) */
+    int lead = e - 1;        /* exponent of the leading bit */
+    if (lead < emin) lead = emin;   /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, lead - (prec - 1));
+    double r = nearbyint(a / quantum) * quantum;   /* default mode: ties to even */
+    double max_finite = ldexp(2.0 - ldexp(1.0, 1 - prec), emax);
+    if (r > max_finite) r = INFINITY;
+    return v < 0 ? -r : r;
+}
+
+static double round_to_dtype(double v, int dt) {
+    switch (dt) {
+    case OR_F16:  return round_to_format(v, 11, -14, 15);
+    case OR_BF16: return round_to_format(v, 8, -126, 127);
+    default:      return round_to_format(v, 24, -126, 127);
+    }
+}
+
+static uint16_t double_to_bf16_bits(double v) {
+    if (v != v) return 0x7fc0;
+    double r = round_to_format(v, 8, -126, 127);   /* representable in binary32 */
+    float f = (float)r;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+static uint16_t double_to_half_bits(double v) {
+    if (v != v) return 0x7e00;
+    double r = round_to_format(v, 11, -14, 15);
+    uint16_t sign = signbit(r) ? 0x8000 : 0;
+    double a = fabs(r);
+    if (isinf(a)) return sign | 0x7c00;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);
+    int lead = e - 1;
+    if (lead < -14)                              /* subnormal: a = m * 2^-24 */
+        return sign | (uint16_t)(a * 16777216.0);
+    uint16_t m = (uint16_t)((ldexp(a, -lead) - 1.0) * 1024.0);
+    return sign | (uint16_t)((lead + 15) << 10) | m;
+}
+
+/* Value of element i of an array of dtype dt. */
+static double load_elem(const void* base, int64_t i, int dt) {
+    if (dt == OR_F32) {
+        float f;
+        memcpy(&f, (const char*)base + 4 * i, 4);
+        return (double)f;
+    }
+    uint16_t h;
+    memcpy(&h, (const char*)base + 2 * i, 2);
+    return dt == OR_F16 ? half_bits_to_double(h) : bf16_bits_to_double(h);
+}
+
+/* Store v, rounded to nearest-even, as element i of an array of dtype dt. */
+static void store_elem(void* base, int64_t i, int dt, double v) {
+    if (dt == OR_F32) {
+        float f = (float)v;   /* C conversion: round to nearest-even */
+        memcpy((char*)base + 4 * i, &f, 4);
+    } else {
+        uint16_t h = dt == OR_F16 ? double_to_half_bits(v) : double_to_bf16_bits(v);
+        memcpy((char*)base + 2 * i, &h, 2);
+    }
+}
+
+/* --- exported format helpers (used by the tests and the gate) ------------ */
+
+void oracle_decode(const void* src, int dt, int64_t n, double* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(src, i, dt);
+}
+
+void oracle_encode(const double* src, int64_t n, int dt, void* dst) {
+    for (int64_t i = 0; i < n; ++i) store_elem(dst, i, dt, src[i]);
+}
+
+/* dst[i] = value of src[i] after rounding into dtype dt (the gate's rounding floor). */
+void oracle_round(const double* src, int64_t n, int dt, double* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = round_to_dtype(src[i], dt);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Golden: fp64 throughout                                                   */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * y[M*N] (fp64), rstd[M] (fp64). gamma has dtype dt like x.
+ * Forward formula: "Problem and reference formula" (r and y); offset variant from
+ * the torchtitan page's golden implementation, (1 + w) * x * r.
+ */
+void oracle_fwd_golden(const void* x, const void* gamma, int64_t M, int64_t N,
+                       double eps, int dt, int offset, double* y, double* rstd) {
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(x, row + j, dt);
+            ss += xv * xv;
+        }
+        double r = 1.0 / sqrt(ss / (double)N + eps);
+        if (rstd) rstd[i] = r;
+        if (!y) continue;
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(x, row + j, dt);
+            double w = load_elem(gamma, j, dt);
+            y[row + j] = offset ? (1.0 + w) * xv * r : xv * r * w;
+        }
+    }
+}
+
+/*
+ * dx[M*N] (fp64, may be NULL to skip), dgamma[N] (fp64, may be NULL).
+ * r is recomputed from x exactly as in the forward pass.
+ * Backward formula: "Why do we need a forward and a backward pass?" with
+ * u = dy * gamma, dx = r*u - x*r^3*mean(u*x); dgamma = sum over rows of dy*x*r.
+ */
+void oracle_bwd_golden(const void* dy, const void* x, const void* gamma, int64_t M,
+                       int64_t N, double eps, int dt, int offset, double* dx,
+                       double* dgamma) {
+    if (dgamma)
+        for (int64_t j = 0; j < N; ++j) dgamma[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(x, row + j, dt);
+            ss += xv * xv;
+        }
+        double r = 1.0 / sqrt(ss / (double)N + eps);
+        double sux = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double w = load_elem(gamma, j, dt);
+            double g = offset ? 1.0 + w : w;
+            double u = load_elem(dy, row + j, dt) * g;
+            sux += u * load_elem(x, row + j, dt);
+        }
+        double mean_ux = sux / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = load_elem(x, row + j, dt);
+            double dyv = load_elem(dy, row + j, dt);
+            double w = load_elem(gamma, j, dt);
+            double g = offset ? 1.0 + w : w;
+            double u = dyv * g;
+            if (dx) dx[row + j] = r * u - xv * r * r * r * mean_ux;
+            if (dgamma) dgamma[j] += dyv * xv * r;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Reference: I/O dtype, fp32 intermediates, sequential sums                 */
+/* ------------------------------------------------------------------------- */
+
+static float ld32(const void* base, int64_t i, int dt) {
+    return (float)load_elem(base, i, dt);   /* exact for all three dtypes */
+}
+
+/* fp32 r of one row: sequential sum of squares, mean, add eps, sqrt, reciprocal. */
+static float row_rstd_f32(const void* x, int64_t row, int64_t N, float eps, int dt) {
+    float ss = 0.0f;
+    for (int64_t j = 0; j < N; ++j) {
+        float xv = ld32(x, row + j, dt);
+        float sq = xv * xv;
+        ss = ss + sq;
+    }
+    float ms = ss / (float)N;
+    float den = sqrtf(ms + eps);
+    return 1.0f / den;
+}
+
+/*
+ * y[M*N] in dtype dt, rstd[M] fp32. Multiplication order follows the pages'
+ * reference code: (x * r) * gamma, and for the offset variant ((1 + w) * x) * r.
+ */
+void oracle_fwd_reference(const void* x, const void* gamma, int64_t M, int64_t N,
+                          float eps, int dt, int offset, void* y, float* rstd) {
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        float r = row_rstd_f32(x, row, N, eps, dt);
+        if (rstd) rstd[i] = r;
+        if (!y) continue;
+        for (int64_t j = 0; j < N; ++j) {
+            float xv = ld32(x, row + j, dt);
+            float w = ld32(gamma, j, dt);
+            float out;
+            if (offset) {
+                float g = 1.0f + w;
+                float gx = g * xv;
+                out = gx * r;
+            } else {
+                float xr = xv * r;
+                out = xr * w;
+            }
+            store_elem(y, row + j, dt, (double)out);
+        }
+    }
+}
+
+/*
+ * dx[M*N] in dtype dt (may be NULL), dgamma[N] in dtype dt (may be NULL).
+ * r is recomputed in fp32 from x exactly as oracle_fwd_reference does.
+ * dx = (r * u) - ((x * r^3) * c) with r^3 = (r * r) * r and c = (sum u*x) / N;
+ * dgamma accumulates (dy * x) * r over rows in row order, in one fp32 sum per
+ * column, and is rounded into dtype dt once at the end.
+ */
+void oracle_bwd_reference(const void* dy, const void* x, const void* gamma, int64_t M,
+                          int64_t N, float eps, int dt, int offset, void* dx,
+                          void* dgamma) {
+    float* acc = NULL;
+    if (dgamma) {
+        acc = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+        for (int64_t j = 0; j < N; ++j) acc[j] = 0.0f;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        float r = row_rstd_f32(x, row, N, eps, dt);
+        float sux = 0.0f;
+        for (int64_t j = 0; j < N; ++j) {
+            float w = ld32(gamma, j, dt);
+            float g = offset ? 1.0f + w : w;
+            float u = ld32(dy, row + j, dt) * g;
+            float ux = u * ld32(x, row + j, dt);
+            sux = sux + ux;
+        }
+        float c = sux / (float)N;
+        float r2 = r * r;
+        float r3 = r2 * r;
+        for (int64_t j = 0; j < N; ++j) {
+            float xv = ld32(x, row + j, dt);
+            float dyv = ld32(dy, row + j, dt);
+            float w = ld32(gamma, j, dt);
+            float g = offset ? 1.0f + w : w;
+            float u = dyv * g;
+            if (dx) {
+                float t1 = r * u;
+                float xr3 = xv * r3;
+                float t2 = xr3 * c;
+                float d = t1 - t2;
+                store_elem(dx, row + j, dt, (double)d);
+            }
+            if (acc) {
+                float dyx = dyv * xv;
+                float term = dyx * r;
+                acc[j] = acc[j] + term;
+            }
+        }
+    }
+    if (acc) {
+        for (int64_t j = 0; j < N; ++j) store_elem(dgamma, j, dt, (double)acc[j]);
+        free(acc);
+    }
+}
