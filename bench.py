@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark: RMSNorm forward + backward HBM throughput on GB300.
+
+One step = one forward (rmsnorm_fwd) and one backward (rmsnorm_bwd: fused row
+kernel + dgamma column reduction) over the whole workload, inputs resident in
+HBM. Default workload: bf16, M = 65536 rows (8 sequences x 8192 tokens),
+N = 4096, eps = 1e-6, x ~ 3*N(0,1), gamma = 1 + 0.1*N(0,1), dy ~ 1e-2*N(0,1).
+Each tensor is 512 MiB, larger than L2 (129 MB), so no L2 flush is needed
+between steps.
+
+value  = algorithmic bytes of all ranks' steps / max-over-ranks time, in GB/s,
+         where fwd bytes = 2*M*N*s + N*s + 4*M and bwd bytes = 3*M*N*s + 2*N*s + 4*M.
+e2e    = the same metric through the C ABI with host buffers: each step copies
+         x, gamma, dy from pinned host memory, runs both passes, and copies
+         y, rstd, dx, dgamma back.
+roofline = the backward pass (the dominant cost) against the measured HBM copy
+         bandwidth in MEASURED_PEAKS.json.
+cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
+         fp32-intermediate reference) on a bounded row sample of the workload.
+
+Multi-GPU (torchrun): one process per GPU, each running an independent replica
+of the workload (weak scaling); there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "RMSNorm fwd/bwd HBM GB/s & % of peak, bf16 M=65536 N=4096, 1 GB300"
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing (also exercised on CPU with gloo by the tests)
+# --------------------------------------------------------------------------- #
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_step_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step_per_rank * steps / max_seconds / 1e9
+
+
+# --------------------------------------------------------------------------- #
+# clocks
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t_start: float, t_end: float):
+        del t_start, t_end
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- #
+# helpers
+# --------------------------------------------------------------------------- #
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "rmsnorm_fwd_bwd_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_digest") != kernel_source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def cpu_oracle_rate(w, x, g, dy, budget_s: float):
+    """Time the oracle's fp32-intermediate reference (fwd + bwd) on a row sample sized
+    to about budget_s seconds. Returns (GB/s of algorithmic bytes, rows, seconds)."""
+    from oracle import oracle as orc
+    s = w.elem_bytes
+
+    def run(rows):
+        xs, dys = x[:rows], dy[:rows]
+        t = time.perf_counter()
+        orc.fwd_reference(xs, g, w.dtype, eps=w.eps, offset=w.offset)
+        orc.bwd_reference(dys, xs, g, w.dtype, eps=w.eps, offset=w.offset)
+        return time.perf_counter() - t
+
+    probe = min(64, w.M)
+    t = run(probe)
+    rows = int(min(w.M, max(probe, probe * budget_s / max(t, 1e-6))))
+    t = run(rows)
+    nbytes = (2 * rows * w.N * s + w.N * s + 4 * rows) + (3 * rows * w.N * s + 2 * w.N * s + 4 * rows)
+    return nbytes / t / 1e9, rows, t
+
+
+# --------------------------------------------------------------------------- #
+# the reference arm: the CPU oracle
+# --------------------------------------------------------------------------- #
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import oracle as orc
+    from rmsnorm_fwd_bwd_gb300 import inputs
+    x, g, dy = inputs.workload_inputs(w)
+    orc.build()
+    s = w.elem_bytes
+    total_budget = 60.0
+    probe = 64
+    t0 = time.perf_counter()
+    orc.fwd_reference(x[:probe], g, w.dtype, eps=w.eps, offset=w.offset)
+    orc.bwd_reference(dy[:probe], x[:probe], g, w.dtype, eps=w.eps, offset=w.offset)
+    per_row = (time.perf_counter() - t0) / probe
+    rows = int(max(1, min(w.M, total_budget / max(args.steps + args.warmup, 1) / max(per_row, 1e-9))))
+    starts = [(i * rows) % max(1, w.M - rows + 1) for i in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        a = starts[i]
+        orc.fwd_reference(x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+        orc.bwd_reference(dy[a:a + rows], x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        a = starts[i]
+        orc.fwd_reference(x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+        orc.bwd_reference(dy[a:a + rows], x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+    dt = time.perf_counter() - t0
+    nbytes = (2 * rows * w.N * s + w.N * s + 4 * rows) + (3 * rows * w.N * s + 2 * w.N * s + 4 * rows)
+    value = nbytes * args.steps / dt / 1e9
+    sample = f"{rows} consecutive rows of the {w.M}x{w.N} workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"RMSNorm fwd+bwd {w.dtype} M={w.M} N={w.N} eps={w.eps:g}"
+                        + (" offset" if w.offset else ""),
+            "name": w.name, "M": w.M, "N": w.N, "io_dtype": w.dtype, "offset": w.offset,
+            "l2": "inputs larger than L2 (no flush)" if w.M * w.N * w.elem_bytes > 129e6
+            else "L2 flushed between steps",
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    from rmsnorm_fwd_bwd_gb300 import binding as B
+    from rmsnorm_fwd_bwd_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    dt = w.dtype
+    M, N = w.M, w.N
+
+    x_np, g_np, dy_np = inputs.workload_inputs(w)
+    x_h = B.to_device(x_np.reshape(-1), dt, "cpu").pin_memory()
+    g_h = B.to_device(g_np, dt, "cpu").pin_memory()
+    dy_h = B.to_device(dy_np.reshape(-1), dt, "cpu").pin_memory()
+    x = x_h.to(dev).view(M, N)
+    g = g_h.to(dev)
+    dy = dy_h.to(dev).view(M, N)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dg = torch.empty_like(g)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    wsz = B.rmsnorm_bwd_workspace_size(M, N, dt)
+    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+    flush = None
+    if M * N * w.elem_bytes < 256e6:
+        flush = torch.empty(int(512e6), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        st = B.rmsnorm_fwd(x, g, y, rstd, M, N, w.eps, dt, int(w.offset), stream)
+        if st:
+            raise B.RMSNormError(st, "rmsnorm_fwd")
+
+    def bwd():
+        st = B.rmsnorm_bwd(dy, x, g, rstd, dx, dg, M, N, dt, int(w.offset), ws, wsz, stream)
+        if st:
+            raise B.RMSNormError(st, "rmsnorm_bwd")
+
+    B.rmsnorm_device_error(clear=True)
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    if flush is None:
+        total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    else:
+        total_ms = sum(ev[k][0].elapsed_time(ev[k][2]) for k in range(K))
+    fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    dev_err = B.rmsnorm_device_error(clear=True)
+
+    secs = max_over_ranks(total_ms / 1e3, world, device=dev)
+    step_bytes = w.fwd_bytes() + w.bwd_bytes()
+    value = aggregate(step_bytes, K, world, secs)
+
+    # end to end through the C ABI with host buffers
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    dg_h = torch.empty_like(g_h).pin_memory()
+    r_h = torch.empty(M, dtype=torch.float32).pin_memory()
+    xf, gf, dyf = x.view(-1), g, dy.view(-1)
+    e2e_steps = max(3, min(K, args.e2e_steps))
+
+    def e2e_step():
+        xf.copy_(x_h, non_blocking=True)
+        gf.copy_(g_h, non_blocking=True)
+        dyf.copy_(dy_h, non_blocking=True)
+        fwd()
+        bwd()
+        y_h.copy_(y.view(-1), non_blocking=True)
+        r_h.copy_(rstd, non_blocking=True)
+        dx_h.copy_(dx.view(-1), non_blocking=True)
+        dg_h.copy_(dg, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
+    h2d = (x_h.numel() + g_h.numel() + dy_h.numel()) * w.elem_bytes
+    d2h = (y_h.numel() + dx_h.numel() + dg_h.numel()) * w.elem_bytes + 4 * M
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    bwd_avg_ms = statistics.mean(bwd_ms)
+    fwd_avg_ms = statistics.mean(fwd_ms)
+    bwd_gbs = w.bwd_bytes() / (bwd_avg_ms / 1e3) / 1e9
+    fwd_gbs = w.fwd_bytes() / (fwd_avg_ms / 1e3) / 1e9
+    traffic = recorded_traffic(f"rmsnorm_bwd {w.name}")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if dt == "float32" else
+        {"bfloat16": "bf16", "float16": "f16"}[dt],
+        "data": "synthetic (seeded; see rmsnorm_fwd_bwd_gb300/inputs.py)",
+        "config": workload_config(w),
+        "fwd": {"us": fwd_avg_ms * 1e3, "gbs": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
+                "bytes": w.fwd_bytes(), "plan": B.rmsnorm_describe_plan(0, M, N, dt)},
+        "bwd": {"us": bwd_avg_ms * 1e3, "gbs": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
+                "bytes": w.bwd_bytes(), "plan": B.rmsnorm_describe_plan(1, M, N, dt)},
+        "roofline": {"bound": "hbm", "kernel": "rmsnorm_bwd (fused row kernel + dgamma reduce)",
+                     "achieved": bwd_gbs, "peak": peak, "peak_kind": f"{peak_kind} HBM copy",
+                     "unit": "GB/s", "frac": bwd_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes": w.bwd_bytes()},
+        "e2e": {"value": step_bytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 3 * K,
+        "device_error_word": dev_err,
+        "clocks": clocks.summary(0, 0),
+    }
+    if not args.no_cpu_baseline:
+        rate, rows, t = cpu_oracle_rate(w, x_np, g_np, dy_np, args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {rows} rows of the workload, fwd+bwd reference, "
+                                          f"{t:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the headline)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from rmsnorm_fwd_bwd_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm.so: row-wise RMSNorm forward and backward on
+ * one NVIDIA GB300 (sm_103a), hand-written CUDA kernels.
+ *
+ * Operation (page "Check an AI model calculation before accelerating it",
+ * sections "Problem and reference formula" and "Why do we need a forward and a
+ * backward pass?"; offset variant from the page "torchtitan kernel numerics
+ * verification", section on the golden / reference / target implementations).
+ * For each row i of an M x N matrix x:
+ *
+ *     r_i      = 1 / sqrt(mean_j(x_ij^2) + eps)
+ *     y_ij     = x_ij * r_i * g_j            g = gamma, or (1 + gamma) with offset
+ *     u_ij     = dy_ij * g_j
+ *     dx_ij    = r_i * u_ij - x_ij * r_i^3 * mean_j(u_ij * x_ij)
+ *     dgamma_j = sum_i dy_ij * x_ij * r_i    (a sum over rows, not a mean)
+ *
+ * Means divide by the logical N. All arithmetic is fp32 whatever the I/O dtype;
+ * inputs are converted at load and each output element is rounded once, to
+ * nearest-even, into the I/O dtype. dgamma is deterministic: fp32 partial sums
+ * per persistent thread block, then one fixed-order column reduction (no
+ * floating-point atomics), so repeated calls on the same device give identical
+ * bits.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers on the current CUDA device. The
+ *     caller owns every buffer and the stream; the library allocates nothing
+ *     and keeps no state between calls apart from launch-configuration caches
+ *     and the device error word (rmsnorm_device_error).
+ *   - Layout: dense row-major, row pitch = N elements. x, y, dy, dx, gamma and
+ *     dgamma share the I/O dtype; rstd is float32[M]. Outputs must not overlap
+ *     inputs.
+ *   - Pointers must be aligned to their element size. Rows whose byte length is
+ *     a multiple of 16 with 16-byte-aligned x/y/dy/dx/gamma take the TMA bulk-copy
+ *     path; anything else takes a general path with scalar loads. Both give
+ *     results within the same correctness gate.
+ *   - All calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     Validation happens on the host before any launch; when a call returns an
+ *     error nothing was launched and no output was written. There is no
+ *     fallback to another implementation, on the CPU or elsewhere.
+ *   - 1 <= N <= RMSNORM_MAX_N; 0 <= M <= RMSNORM_MAX_M. M == 0 is valid: the
+ *     forward does nothing and the backward writes dgamma = 0.
+ *   - eps must be finite and > 0 (eps = 0 would turn an all-zero row into 0*inf).
+ *   - offset must be 0 (y = x*r*gamma) or 1 (y = x*r*(1 + gamma)); dgamma has
+ *     the same formula in both cases since d(1 + w)/dw = 1.
+ */
+#ifndef RMSNORM_H
+#define RMSNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so that this header needs
+ * no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st* rmsnorm_stream_t;
+
+#define RMSNORM_MAX_N 16384
+#define RMSNORM_MAX_M 2147483647LL
+
+typedef enum {
+    RMSNORM_F32 = 0,  /* IEEE binary32 */
+    RMSNORM_F16 = 1,  /* IEEE binary16 */
+    RMSNORM_BF16 = 2  /* bfloat16 */
+} rmsnorm_dtype;
+
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_NULL = 1,        /* a required pointer is NULL */
+    RMSNORM_ERR_SHAPE = 2,       /* M or N out of range */
+    RMSNORM_ERR_DTYPE = 3,       /* dtype is not one of rmsnorm_dtype */
+    RMSNORM_ERR_EPS = 4,         /* eps not finite or not > 0 */
+    RMSNORM_ERR_ALIGN = 5,       /* a pointer is not aligned as required */
+    RMSNORM_ERR_WORKSPACE = 6,   /* workspace smaller than rmsnorm_bwd_workspace_size */
+    RMSNORM_ERR_UNSUPPORTED = 7, /* no kernel for this configuration */
+    RMSNORM_ERR_CUDA = 8,        /* a CUDA runtime call or launch failed */
+    RMSNORM_ERR_ARG = 9          /* another argument is invalid (offset not 0/1) */
+} rmsnorm_status;
+
+/*
+ * Forward. Reads x[M*N] and gamma[N] (dtype), writes y[M*N] (dtype) and
+ * rstd[M] (float32, r_i above; keep it for the backward).
+ * x, gamma, y, rstd may be NULL only when M == 0.
+ */
+rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                           int64_t M, int64_t N, float eps, rmsnorm_dtype dtype,
+                           int offset, rmsnorm_stream_t stream);
+
+/*
+ * Bytes of device workspace rmsnorm_bwd needs for this shape on the CURRENT
+ * device (it depends on the device's SM count). The workspace holds float32
+ * dgamma partial sums, one row of N per persistent block (or cluster); it must
+ * be 16-byte aligned. Returns 0 when M == 0 or when an argument is invalid
+ * (rmsnorm_bwd then reports the precise error). Host-only; launches nothing.
+ */
+size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype);
+
+/*
+ * Backward. Reads dy[M*N], x[M*N], gamma[N] (dtype) and rstd[M] (float32 from
+ * rmsnorm_fwd on the same x and eps; not validated), writes dx[M*N] and
+ * dgamma[N] (dtype). Two launches on `stream`: the fused row kernel (dx and
+ * per-block dgamma partials into `workspace`) and the column reduction.
+ * `workspace` must hold at least rmsnorm_bwd_workspace_size(M, N, dtype)
+ * bytes (it may be NULL when that is 0). The workspace is scratch: its contents
+ * on entry are ignored and on return are unspecified.
+ */
+rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
+                           const float* rstd, void* dx, void* dgamma,
+                           int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
+                           void* workspace, size_t workspace_bytes,
+                           rmsnorm_stream_t stream);
+
+/* Static English text for a status code; never NULL. */
+const char* rmsnorm_status_string(rmsnorm_status status);
+
+/*
+ * Device error word of the CURRENT device. Kernels that wait on an mbarrier
+ * give up after a bounded number of polls, set bit 0 of this word and skip
+ * their stores, so a hang becomes a reported error. Reading synchronizes the
+ * device. *flags receives the word; clear != 0 resets it to 0.
+ */
+rmsnorm_status rmsnorm_device_error(uint32_t* flags, int clear);
+
+/*
+ * Launch plan the library would use, as text (for logs and tests), e.g.
+ * "tma cluster=1 threads=256 vpt=2 stages=6 blocks=456". pass: 0 = forward,
+ * 1 = backward. aligned16: whether the data pointers will be 16-byte aligned.
+ * Writes at most buf_len bytes including the terminating NUL. Host-only.
+ */
+rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,
+                                     int aligned16, char* buf, size_t buf_len);
+
+/*
+ * Tuning hook: override the TMA-path launch shape for one pass (0 = forward,
+ * 1 = backward). threads: threads per block (multiple of 32); vpt: 16-byte
+ * vectors per thread (1, 2, 4 or 8); stages: pipeline depth; blocks_per_sm:
+ * cap on resident blocks per SM. Any value 0 keeps the built-in choice;
+ * all zeros restores the defaults. A shape that cannot hold the row makes the
+ * following calls fail with RMSNORM_ERR_UNSUPPORTED. Process-wide, not
+ * thread-safe against concurrent calls.
+ */
+rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int stages,
+                                           int blocks_per_sm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_H */

@@ -22,7 +22,12 @@ condition number of reductions and the report table):
 
 The constants are declared here, before any target runs, and are never changed
 to make a failing target pass.  For float32 I/O an additional normwise bound
-max|target - golden| / max|golden| <= FP32_MAX_RELATIVE_ERROR applies.
+max|target - golden| / max|golden| <= FP32_MAX_RELATIVE_ERROR applies. Where
+the fp32-intermediate reference itself misses that bound (an ill-conditioned
+tensor, e.g. dx for N = 1, where dx = r*u*eps/(x^2 + eps) cancels almost
+completely), the bound cannot tell a bug from rounding; the verdict then rests
+on step 4 and is "PASS WITH LIMITATIONS", the page's verdict for results that
+follow the same conditioning-driven noise envelope as the reference.
 """
 from __future__ import annotations
 
@@ -124,12 +129,23 @@ def check(tensor: str, golden: np.ndarray, reference: np.ndarray, target: np.nda
     ok = res.target_error <= res.threshold
     if not ok:
         res.notes.append(f"target_error {res.target_error:.3e} > threshold {res.threshold:.3e}")
+    limited = False
     if rel_bound is not None and res.golden_scale > 0:
         rel = res.target_error / res.golden_scale
+        ref_rel = res.reference_error / res.golden_scale
         if rel > rel_bound:
-            ok = False
-            res.notes.append(f"normwise relative error {rel:.3e} > {rel_bound:.1e}")
-    res.verdict = "PASS" if ok else "FAIL"
+            if ref_rel > rel_bound and ok:
+                # The fp32-intermediate reference itself misses the bound: the
+                # tensor is too ill-conditioned for it to separate a bug from
+                # rounding, so (as in the conditioning check) the verdict rests
+                # on the main gate alone and is reported with that limitation.
+                limited = True
+                res.notes.append(f"normwise relative error {rel:.3e} > {rel_bound:.1e}, but the "
+                                 f"reference itself is at {ref_rel:.3e}: bound not attainable here")
+            else:
+                ok = False
+                res.notes.append(f"normwise relative error {rel:.3e} > {rel_bound:.1e}")
+    res.verdict = ("PASS WITH LIMITATIONS" if limited else "PASS") if ok else "FAIL"
     return res
 
 
@@ -139,6 +155,8 @@ def overall(results) -> str:
         return "FAIL"
     if any(v == "INCONCLUSIVE" for v in verdicts):
         return "INCONCLUSIVE"
+    if any(v == "PASS WITH LIMITATIONS" for v in verdicts):
+        return "PASS WITH LIMITATIONS"
     return "PASS"
 
 

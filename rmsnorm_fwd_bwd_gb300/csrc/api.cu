@@ -1,0 +1,384 @@
+// api.cu -- the C ABI declared in include/rmsnorm.h: argument validation, launch
+// planning (path, cluster size, threads, pipeline depth, persistent grid size
+// from the device's SM count and occupancy) and kernel launches.
+//
+// Argument contract (page "Check an AI model calculation before accelerating
+// it", section "The memory contract is part of the computation"): inputs are
+// checked before any output is written and unsupported inputs are rejected
+// rather than routed to another implementation (section "Adapting the kernel
+// and moving to production": no silent fallback).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/rmsnorm.h"
+#include "launch.h"
+
+namespace rmsnorm {
+
+__device__ uint32_t g_device_error;  // see rmsnorm_device_error
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per tensor
+constexpr int kRingBudgetBytes = 65536;  // default TMA ring size per CTA
+constexpr int kMaxStages = 8;
+constexpr int kDefaultThreadCap = 256;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    uint32_t* err = nullptr;
+};
+
+struct Override {
+    int threads = 0, vpt = 0, stages = 0, blocks_per_sm = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+Override g_override[2];
+unsigned g_override_gen = 0;
+std::map<std::tuple<int, int, int64_t, int, int, int, int, unsigned>, Plan> g_plans;
+std::map<std::pair<const void*, int>, bool> g_attr_done;
+
+int elem_bytes(int dt) { return dt == RMSNORM_F32 ? 4 : 2; }
+int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Caller holds g_mu.
+bool device_info(int dev, DeviceInfo*& out) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return false;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return false;
+        d.err = static_cast<uint32_t*>(p);
+        d.ready = true;
+    }
+    out = &d;
+    return true;
+}
+
+// Caller holds g_mu. Allows the largest dynamic shared memory once per kernel and device.
+bool prepare_kernel(const void* k, int dev, const DeviceInfo& di) {
+    auto key = std::make_pair(k, dev);
+    if (g_attr_done.count(key)) return true;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return false;
+    const int dyn_max = di.smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
+        return false;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return false;
+    g_attr_done[key] = true;
+    return true;
+}
+
+// Resident blocks per SM (cluster == 1) or resident clusters on the device.
+bool occupancy_units(const void* k, const Plan& p, const DeviceInfo& di, int cap_per_sm, int64_t& units) {
+    if (p.cluster == 1) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, p.threads, p.smem) != cudaSuccess) return false;
+        if (cap_per_sm > 0 && n > cap_per_sm) n = cap_per_sm;
+        if (n < 1) return false;
+        units = static_cast<int64_t>(n) * di.sms;
+        return true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * di.sms), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) return false;
+    if (cap_per_sm > 0) {
+        const int cap = cap_per_sm * di.sms / p.cluster;
+        if (n > cap) n = cap;
+    }
+    if (n < 1) return false;
+    units = n;
+    return true;
+}
+
+// TMA path: rows whose byte length is a multiple of 16, split over a cluster so
+// that one CTA stages at most kSliceMaxBytes per tensor.
+bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    const int s = elem_bytes(dt);
+    const int vec = 16 / s;
+    if ((static_cast<int64_t>(N) * s) % 16 != 0) return false;
+    int cl = 1;
+    while (cl <= 4 && !((static_cast<int64_t>(N) * s) / cl <= kSliceMaxBytes && N % (cl * vec) == 0)) cl *= 2;
+    if (cl > 4) return false;
+    const int nvec = N / (cl * vec);
+    const Override& ov = g_override[pass];
+    int vpt = ov.vpt;
+    if (vpt == 0) {
+        const int cap = ov.threads ? ov.threads : kDefaultThreadCap;
+        for (vpt = 1; vpt <= 8; vpt *= 2)
+            if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
+        if (vpt > 8) return false;
+    }
+    if (vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8) return false;
+    int threads = ov.threads ? ov.threads : static_cast<int>(round_up(ceil_div(nvec, vpt), 32));
+    if (threads < 32) threads = 32;
+    if (threads % 32 != 0 || threads > kTmaMaxThreads) return false;
+    if (static_cast<int64_t>(threads) * vpt < nvec) return false;
+    if ((threads / 32) * cl > 32) return false;
+    const int slice = (N / cl) * s;
+    const int stage = (pass == 0 ? 1 : 2) * slice;
+    const int fixed = 2 * 32 * 4 + 16;
+    int stages = ov.stages ? ov.stages : kRingBudgetBytes / stage;
+    if (stages > kMaxStages && !ov.stages) stages = kMaxStages;
+    if (stages < 2) stages = 2;
+    while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
+    if (stages < 1) return false;
+    p.path = kPathTma;
+    p.dtype = dt;
+    p.offset = offset;
+    p.cluster = cl;
+    p.threads = threads;
+    p.per_thread = vpt;
+    p.stages = stages;
+    p.smem = static_cast<size_t>(stages) * (stage + 8) + fixed;
+    const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
+    if (!k || !prepare_kernel(k, dev, di)) return false;
+    int64_t units = 0;
+    if (!occupancy_units(k, p, di, ov.blocks_per_sm, units)) return false;
+    p.units = units < M ? units : M;
+    return true;
+}
+
+// General path: any N (<= RMSNORM_MAX_N) and element alignment, one CTA per row.
+bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    int ept = 1;
+    while (ept < kScalarMaxPerThread && round_up(ceil_div(N, ept), 32) > kScalarMaxThreads) ept *= 2;
+    const int threads = static_cast<int>(round_up(ceil_div(N, ept), 32));
+    if (threads > kScalarMaxThreads) return false;
+    p.path = kPathScalar;
+    p.dtype = dt;
+    p.offset = offset;
+    p.cluster = 1;
+    p.threads = threads;
+    p.per_thread = ept;
+    p.stages = 0;
+    p.smem = pass == 0 ? 0 : static_cast<size_t>(N) * 4;
+    const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
+    if (!k || !prepare_kernel(k, dev, di)) return false;
+    int64_t units = 0;
+    if (!occupancy_units(k, p, di, 0, units)) return false;
+    p.units = units < M ? units : M;
+    return true;
+}
+
+// Caller holds g_mu.
+bool get_plan(int pass, int64_t M, int N, int dt, int offset, bool aligned16, int dev, const DeviceInfo& di,
+              Plan& p) {
+    const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
+    const int path = (aligned16 && tma_shape) ? kPathTma : kPathScalar;
+    auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, 0, g_override_gen);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+        p = it->second;
+        return true;
+    }
+    const bool ok = path == kPathTma ? plan_tma(pass, M, N, dt, offset, dev, di, p)
+                                     : plan_scalar(pass, M, N, dt, offset, dev, di, p);
+    if (!ok) {
+        (void)cudaGetLastError();  // leave no stale runtime error behind
+        return false;
+    }
+    if (g_plans.size() > 4096) g_plans.clear();
+    g_plans[key] = p;
+    return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+rmsnorm_status check_common(int64_t M, int64_t N, rmsnorm_dtype dt, int offset) {
+    if (dt != RMSNORM_F32 && dt != RMSNORM_F16 && dt != RMSNORM_BF16) return RMSNORM_ERR_DTYPE;
+    if (offset != 0 && offset != 1) return RMSNORM_ERR_ARG;
+    if (M < 0 || M > RMSNORM_MAX_M || N < 1 || N > RMSNORM_MAX_N) return RMSNORM_ERR_SHAPE;
+    return RMSNORM_OK;
+}
+
+rmsnorm_status current_device(int& dev, DeviceInfo*& di) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (!device_info(dev, di)) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+}  // namespace rmsnorm
+
+using namespace rmsnorm;
+
+extern "C" rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
+                                      int64_t N, float eps, rmsnorm_dtype dtype, int offset,
+                                      rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, offset);
+    if (st != RMSNORM_OK) return st;
+    if (!std::isfinite(eps) || !(eps > 0.0f)) return RMSNORM_ERR_EPS;
+    if (M == 0) return RMSNORM_OK;
+    if (!x || !gamma || !y || !rstd) return RMSNORM_ERR_NULL;
+    const size_t s = elem_bytes(dtype);
+    if (!aligned(x, s) || !aligned(gamma, s) || !aligned(y, s) || !aligned(rstd, 4)) return RMSNORM_ERR_ALIGN;
+    const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(0, M, static_cast<int>(N), dtype, offset, a16, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.y = y;
+    a.rstd_out = rstd;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.eps = eps;
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_fwd(p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+extern "C" size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype) {
+    if (check_common(M, N, dtype, 0) != RMSNORM_OK || M == 0) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (current_device(dev, di) != RMSNORM_OK) return 0;
+    int64_t units = 0;
+    Plan p;
+    for (int a16 = 0; a16 < 2; ++a16)
+        for (int off = 0; off < 2; ++off)
+            if (get_plan(1, M, static_cast<int>(N), dtype, off, a16 != 0, dev, *di, p) && p.units > units)
+                units = p.units;
+    return static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+}
+
+extern "C" rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
+                                      void* dx, void* dgamma, int64_t M, int64_t N, rmsnorm_dtype dtype,
+                                      int offset, void* workspace, size_t workspace_bytes,
+                                      rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, offset);
+    if (st != RMSNORM_OK) return st;
+    if (!dgamma) return RMSNORM_ERR_NULL;
+    const size_t s = elem_bytes(dtype);
+    if (!aligned(dgamma, s)) return RMSNORM_ERR_ALIGN;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (M == 0) {
+        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
+    if (!dy || !x || !gamma || !rstd || !dx || !workspace) return RMSNORM_ERR_NULL;
+    if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(rstd, 4) ||
+        !aligned(workspace, 16))
+        return RMSNORM_ERR_ALIGN;
+    const bool a16 = aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16);
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, a16, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.dy = dy;
+    a.rstd_in = rstd;
+    a.dx = dx;
+    a.ws = static_cast<float*>(workspace);
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_bwd(p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+extern "C" const char* rmsnorm_status_string(rmsnorm_status status) {
+    switch (status) {
+    case RMSNORM_OK: return "ok";
+    case RMSNORM_ERR_NULL: return "a required pointer is NULL";
+    case RMSNORM_ERR_SHAPE: return "M or N out of range";
+    case RMSNORM_ERR_DTYPE: return "unknown dtype";
+    case RMSNORM_ERR_EPS: return "eps must be finite and > 0";
+    case RMSNORM_ERR_ALIGN: return "pointer not aligned as required";
+    case RMSNORM_ERR_WORKSPACE: return "workspace smaller than rmsnorm_bwd_workspace_size";
+    case RMSNORM_ERR_UNSUPPORTED: return "no kernel for this configuration";
+    case RMSNORM_ERR_CUDA: return "CUDA runtime call or launch failed";
+    case RMSNORM_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+    }
+}
+
+extern "C" rmsnorm_status rmsnorm_device_error(uint32_t* flags, int clear) {
+    if (!flags) return RMSNORM_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(flags, g_device_error, sizeof(uint32_t)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (clear) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    }
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,
+                                                int aligned16, char* buf, size_t buf_len) {
+    if (pass != 0 && pass != 1) return RMSNORM_ERR_ARG;
+    rmsnorm_status st = check_common(M, N, dtype, 0);
+    if (st != RMSNORM_OK) return st;
+    if (!buf || buf_len == 0) return RMSNORM_ERR_NULL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(pass, M > 0 ? M : 1, static_cast<int>(N), dtype, 0, aligned16 != 0, dev, *di, p))
+        return RMSNORM_ERR_UNSUPPORTED;
+    if (p.path == kPathTma)
+        snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.cluster,
+                 p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
+    else
+        snprintf(buf, buf_len, "scalar threads=%d ept=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
+                 static_cast<long long>(p.units), p.smem, di->sms);
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int stages,
+                                                      int blocks_per_sm) {
+    if (pass != 0 && pass != 1) return RMSNORM_ERR_ARG;
+    if (threads < 0 || threads > 1024 || threads % 32 != 0 || stages < 0 || stages > 64 || blocks_per_sm < 0 ||
+        (vpt != 0 && vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8))
+        return RMSNORM_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_override[pass].threads = threads;
+    g_override[pass].vpt = vpt;
+    g_override[pass].stages = stages;
+    g_override[pass].blocks_per_sm = blocks_per_sm;
+    ++g_override_gen;
+    return RMSNORM_OK;
+}

@@ -1,0 +1,371 @@
+// bwd.cu -- RMSNorm backward kernels.
+//
+// Per row, with r the saved forward value and g = gamma (or 1 + w):
+//     u = dy * g;   c = sum_j(u_j * x_j) / N;   dx = (r * u) - ((x * r^3) * c)
+// and, per column, dgamma_j = sum over rows of (dy_j * x_j) * r
+// (page "Check an AI model calculation before accelerating it", sections
+// "Input backward pass: keep the right N", "Where does the cube of r come
+// from?" and "Reducing dgamma without a write race").
+//
+// The row pass is one fused kernel: x and dy are read once (TMA ring as in the
+// forward), dx is written, and each persistent block keeps fp32 dgamma
+// accumulators for its fixed columns in registers across all of its rows. At the
+// end each block (cluster) writes one row of partials to the workspace. A second
+// kernel sums the partial rows per column in a fixed order, so dgamma is
+// deterministic and no floating-point atomics are used (the page's own reason
+// for private partial rows followed by a column pass). The workspace is
+// units x N floats, units ~ 2-3 x #SMs, instead of one row of partials per
+// input row.
+#include "device.cuh"
+#include "launch.h"
+
+namespace rmsnorm {
+
+template <int DT, int VPT, bool OFFSET>
+__global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const uint32_t crank = cluster_rank();
+    const uint32_t csize = cluster_size();
+    const int64_t cid = cluster_id();
+    const int64_t ncl = cluster_count();
+
+    const int ns = a.N / static_cast<int>(csize);
+    const int nvec = ns / VEC;
+    const uint32_t slice_bytes = static_cast<uint32_t>(ns) * E::kBytes;
+    const uint32_t stage_bytes = 2 * slice_bytes;  // x slice, then dy slice
+    const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
+    const int S = a.stages;
+
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
+    float* red = reinterpret_cast<float*>(full + S);
+
+    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+    const size_t slice_off = static_cast<size_t>(crank) * slice_bytes;
+    const char* xsl = static_cast<const char*>(a.x) + slice_off;
+    const char* dysl = static_cast<const char*>(a.dy) + slice_off;
+    char* dxsl = static_cast<char*>(a.dx) + slice_off;
+
+    uint4 g[VPT];
+    {
+        const uint4* gs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.gamma) + slice_off);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nt + tid;
+            g[v] = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    float acc[VPT][VEC];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (csize > 1) cluster_sync();
+
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
+        const size_t off = static_cast<size_t>(cid + j * ncl) * row_bytes;
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_g2s(smem_u32(st), xsl + off, slice_bytes, bar, pol);
+        bulk_g2s(smem_u32(st + slice_bytes), dysl + off, slice_bytes, bar, pol);
+    };
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stage_bytes, smem_u32(&full[j]));
+    }
+
+    float r_next = nrows > 0 ? __ldg(a.rstd_in + cid) : 0.f;
+    bool aborted = false;
+    int64_t abort_row = nrows;
+    for (int64_t j = 0; j < nrows; ++j) {
+        const int s = static_cast<int>(j % S);
+        const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
+        const int64_t row = cid + j * ncl;
+        const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+        const float r = r_next;
+        if (j + 1 < nrows) r_next = __ldg(a.rstd_in + row + ncl);
+
+        bool ok = true;
+        if (!aborted) ok = mbar_wait_bounded(smem_u32(&full[s]), parity, a.err);
+
+        uint4 xv[VPT], dv[VPT];
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nt + tid;
+            if (idx < nvec) {
+                xv[v] = *reinterpret_cast<const uint4*>(st + idx * 16);
+                dv[v] = *reinterpret_cast<const uint4*>(st + slice_bytes + idx * 16);
+            } else {
+                xv[v] = make_uint4(0, 0, 0, 0);
+                dv[v] = make_uint4(0, 0, 0, 0);
+            }
+            float xf[VEC], df[VEC], w[VEC];
+            E::unpack(xv[v], xf);
+            E::unpack(dv[v], df);
+            E::unpack(g[v], w);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float gw = OFFSET ? 1.0f + w[e] : w[e];
+                const float u = __fmul_rn(df[e], gw);
+                if (e & 1) p1 = fmaf(u, xf[e], p1); else p0 = fmaf(u, xf[e], p0);
+                acc[v][e] = fmaf(__fmul_rn(df[e], xf[e]), r, acc[v][e]);
+            }
+        }
+        float* redb = red + (j & 1) * 32;
+        const float wsum = warp_allsum(p0 + p1);
+        if (lane == 0) redb[warp] = wsum;
+        const bool now_aborted = __syncthreads_or(aborted || !ok) != 0;
+        if (now_aborted && !aborted) abort_row = j;
+        aborted = now_aborted;
+        if (csize > 1) cluster_sync();
+
+        if (tid == 0 && !aborted && j + S < nrows) {
+            fence_proxy_async_smem();
+            issue(j + S, st, smem_u32(&full[s]));
+        }
+
+        float t = 0.f;
+        if (csize == 1) {
+            if (lane < nwarps) t = redb[lane];
+        } else if (lane < nwarps * static_cast<int>(csize)) {
+            t = dsmem_ld_f32(dsmem_map(smem_u32(redb + lane % nwarps), lane / nwarps));
+        }
+        t = warp_allsum(t);
+        const float c = t / static_cast<float>(a.N);
+        const float r3 = __fmul_rn(__fmul_rn(r, r), r);
+
+        if (!aborted) {
+            char* dxrow = dxsl + static_cast<size_t>(row) * row_bytes;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int idx = v * nt + tid;
+                if (idx < nvec) {
+                    float xf[VEC], df[VEC], w[VEC], o[VEC];
+                    E::unpack(xv[v], xf);
+                    E::unpack(dv[v], df);
+                    E::unpack(g[v], w);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float gw = OFFSET ? 1.0f + w[e] : w[e];
+                        const float u = __fmul_rn(df[e], gw);
+                        o[e] = __fsub_rn(__fmul_rn(r, u), __fmul_rn(__fmul_rn(xf[e], r3), c));
+                    }
+                    stg128(dxrow + idx * 16, E::pack(o));
+                }
+            }
+        }
+    }
+
+    // one row of dgamma partials per cluster: ws[cid][crank*ns + ...]
+    if (!aborted) {
+        float* wrow = a.ws + static_cast<size_t>(cid) * a.N + static_cast<size_t>(crank) * ns;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nt + tid;
+            if (idx < nvec) {
+#pragma unroll
+                for (int q = 0; q < VEC; q += 4)
+                    *reinterpret_cast<float4*>(wrow + idx * VEC + q) =
+                        make_float4(acc[v][q], acc[v][q + 1], acc[v][q + 2], acc[v][q + 3]);
+            }
+        }
+    }
+    if (csize > 1) cluster_sync();
+    if (aborted && tid == 0) {
+        const int64_t end = abort_row + S < nrows ? abort_row + S : nrows;
+        for (int64_t j = abort_row; j < end; ++j)
+            mbar_wait_bounded(smem_u32(&full[j % S]), static_cast<uint32_t>((j / S) & 1), a.err, 1u << 16);
+    }
+}
+
+// General path: any N, any element alignment. One CTA per row (persistent);
+// thread t owns columns t, t + nt, ...; dgamma accumulators live in shared
+// memory indexed by column (each column is touched by one thread only).
+template <int DT, int EPT, bool OFFSET>
+__global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* acc = reinterpret_cast<float*>(smem);  // [N]
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const int N = a.N;
+
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        const int col = tid + k * nt;
+        if (col < N) acc[col] = 0.f;
+    }
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
+        const int64_t base = row * static_cast<int64_t>(N);
+        const float r = __ldg(a.rstd_in + row);
+        float xv[EPT], dv[EPT];
+        float p = 0.f;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int col = tid + k * nt;
+            if (col < N) {
+                xv[k] = E::ld(a.x, base + col);
+                dv[k] = E::ld(a.dy, base + col);
+                const float w = E::ld(a.gamma, col);
+                const float u = __fmul_rn(dv[k], OFFSET ? 1.0f + w : w);
+                p = fmaf(u, xv[k], p);
+                acc[col] = fmaf(__fmul_rn(dv[k], xv[k]), r, acc[col]);
+            } else {
+                xv[k] = 0.f;
+                dv[k] = 0.f;
+            }
+        }
+        p = warp_allsum(p);
+        if (lane == 0) red[parity][warp] = p;
+        __syncthreads();
+        float t = lane < nwarps ? red[parity][lane] : 0.f;
+        t = warp_allsum(t);
+        const float c = t / static_cast<float>(N);
+        const float r3 = __fmul_rn(__fmul_rn(r, r), r);
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int col = tid + k * nt;
+            if (col < N) {
+                const float w = E::ld(a.gamma, col);
+                const float u = __fmul_rn(dv[k], OFFSET ? 1.0f + w : w);
+                E::st(a.dx, base + col, __fsub_rn(__fmul_rn(r, u), __fmul_rn(__fmul_rn(xv[k], r3), c)));
+            }
+        }
+    }
+    if (blockIdx.x < a.M) {
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int col = tid + k * nt;
+            if (col < N) wrow[col] = acc[col];
+        }
+    }
+}
+
+// dgamma[j] = sum_{p < units} ws[p][j], fixed order: thread (tx, ty) sums rows
+// ty, ty+8, ... of column j in sequence, then the 8 partial sums are added in a
+// fixed tree. units == 0 (no rows) writes zeros.
+template <int DT>
+__global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
+                                                           void* dgamma) {
+    using E = Elem<DT>;
+    __shared__ float part[8][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int col = blockIdx.x * 32 + tx;
+    float s = 0.f;
+    if (col < N) {
+#pragma unroll 4
+        for (int64_t p = ty; p < units; p += 8) s += ws[p * N + col];
+    }
+    part[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && col < N) {
+        const float t = ((part[0][tx] + part[1][tx]) + (part[2][tx] + part[3][tx])) +
+                        ((part[4][tx] + part[5][tx]) + (part[6][tx] + part[7][tx]));
+        E::st(dgamma, col, t);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+template <int DT, bool OFF>
+static const void* bwd_tma_for(int vpt) {
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 4, OFF>);
+    case 8: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 8, OFF>);
+    default: return nullptr;
+    }
+}
+template <int DT, bool OFF>
+static const void* bwd_scalar_for(int ept) {
+    switch (ept) {
+    case 1: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 4, OFF>);
+    case 8: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 8, OFF>);
+    case 16: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 16, OFF>);
+    case 32: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 32, OFF>);
+    default: return nullptr;
+    }
+}
+template <bool OFF>
+static const void* bwd_pick(const Plan& p) {
+    const bool tma = p.path == kPathTma;
+    switch (p.dtype) {
+    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread) : bwd_scalar_for<kF32, OFF>(p.per_thread);
+    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread) : bwd_scalar_for<kF16, OFF>(p.per_thread);
+    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread) : bwd_scalar_for<kBF16, OFF>(p.per_thread);
+    default: return nullptr;
+    }
+}
+
+const void* bwd_kernel(const Plan& p) { return p.offset ? bwd_pick<true>(p) : bwd_pick<false>(p); }
+
+const void* dgamma_reduce_kernel_ptr(int dtype) {
+    switch (dtype) {
+    case kF32: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF32>);
+    case kF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF16>);
+    case kBF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kBF16>);
+    default: return nullptr;
+    }
+}
+
+cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
+    const void* k = bwd_kernel(p);
+    if (!k) return cudaErrorInvalidDeviceFunction;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    RowArgs args = a;
+    void* params[] = {&args};
+    return cudaLaunchKernelExC(&cfg, k, params);
+}
+
+cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
+                                 cudaStream_t s) {
+    const void* k = dgamma_reduce_kernel_ptr(dtype);
+    if (!k) return cudaErrorInvalidDeviceFunction;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), 1, 1);
+    cfg.blockDim = dim3(32, 8, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma};
+    return cudaLaunchKernelExC(&cfg, k, params);
+}
+
+}  // namespace rmsnorm

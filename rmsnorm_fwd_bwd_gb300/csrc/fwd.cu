@@ -1,0 +1,276 @@
+// fwd.cu -- RMSNorm forward kernels.
+//
+// Computes, per row (page "Check an AI model calculation before accelerating
+// it", section "Problem and reference formula"; offset variant from the
+// torchtitan numerics page):
+//     r = 1 / sqrt(sum_j(x_j^2) / N + eps);  y = (x * r) * gamma   or   ((1 + w) * x) * r
+// with x widened to fp32 at load ("Why convert before reducing?") and the mean
+// taken over the logical N, never over a padded width ("N and BLOCK: two sizes
+// you must never confuse").
+//
+// Two kernels:
+//  * fwd_tma_kernel: persistent; each cluster of C CTAs owns rows cid, cid+K, ...
+//    and CTA c of the cluster owns the column slice [c*N/C, (c+1)*N/C). A ring
+//    of `stages` shared-memory buffers is filled by TMA bulk copies
+//    (cp.async.bulk, one per row slice, completion on an mbarrier), so many rows
+//    are in flight per SM without holding them in registers. The sum of squares
+//    is reduced warp -> CTA (shared memory) -> cluster (distributed shared
+//    memory) with one barrier per row; every CTA then forms the same total in the
+//    same order. Output vectors go straight from registers to HBM with 16-byte
+//    coalesced stores.
+//  * fwd_scalar_kernel: any N and any element alignment; one CTA per row,
+//    element-strided scalar loads that stay coalesced across a warp.
+#include "device.cuh"
+#include "launch.h"
+
+namespace rmsnorm {
+
+template <int DT, int VPT, bool OFFSET>
+__global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const uint32_t crank = cluster_rank();
+    const uint32_t csize = cluster_size();
+    const int64_t cid = cluster_id();
+    const int64_t ncl = cluster_count();
+
+    const int ns = a.N / static_cast<int>(csize);  // slice width (elements)
+    const int nvec = ns / VEC;                       // 16-byte vectors per slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(ns) * E::kBytes;
+    const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
+    const int S = a.stages;
+
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice_bytes);
+    float* red = reinterpret_cast<float*>(full + S);  // [2][32] warp partials
+
+    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+    const char* xsl = static_cast<const char*>(a.x) + static_cast<size_t>(crank) * slice_bytes;
+    char* ysl = static_cast<char*>(a.y) + static_cast<size_t>(crank) * slice_bytes;
+
+    // gamma slice, raw, in registers for the whole kernel
+    uint4 g[VPT];
+    {
+        const uint4* gs = reinterpret_cast<const uint4*>(
+            static_cast<const char*>(a.gamma) + static_cast<size_t>(crank) * slice_bytes);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nt + tid;
+            g[v] = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (csize > 1) cluster_sync();  // peers' shared memory is live before any DSMEM read
+
+    const uint64_t pol = l2_evict_first_policy();
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) {
+            const uint32_t bar = smem_u32(&full[j]);
+            mbar_arrive_expect_tx(bar, slice_bytes);
+            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * row_bytes,
+                     slice_bytes, bar, pol);
+        }
+    }
+
+    bool aborted = false;
+    int64_t abort_row = nrows;
+    for (int64_t j = 0; j < nrows; ++j) {
+        const int s = static_cast<int>(j % S);
+        const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
+        const int64_t row = cid + j * ncl;
+        const unsigned char* st = ring + static_cast<size_t>(s) * slice_bytes;
+
+        bool ok = true;
+        if (!aborted) ok = mbar_wait_bounded(smem_u32(&full[s]), parity, a.err);
+
+        uint4 xv[VPT];
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nt + tid;
+            xv[v] = idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0);
+            float f[VEC];
+            E::unpack(xv[v], f);
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                ss0 = fmaf(f[e], f[e], ss0);
+                ss1 = fmaf(f[e + 1], f[e + 1], ss1);
+            }
+        }
+        float* redb = red + (j & 1) * 32;
+        const float wsum = warp_allsum(ss0 + ss1);
+        if (lane == 0) redb[warp] = wsum;
+        // every thread has its slice in registers after this barrier: the stage can refill
+        const bool now_aborted = __syncthreads_or(aborted || !ok) != 0;
+        if (now_aborted && !aborted) abort_row = j;
+        aborted = now_aborted;
+        if (csize > 1) cluster_sync();
+
+        if (tid == 0 && !aborted && j + S < nrows) {
+            fence_proxy_async_smem();
+            const uint32_t bar = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(bar, slice_bytes);
+            bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * row_bytes, slice_bytes, bar, pol);
+        }
+
+        float t = 0.f;
+        if (csize == 1) {
+            if (lane < nwarps) t = redb[lane];
+        } else if (lane < nwarps * static_cast<int>(csize)) {
+            t = dsmem_ld_f32(dsmem_map(smem_u32(redb + lane % nwarps), lane / nwarps));
+        }
+        t = warp_allsum(t);
+        const float ms = t / static_cast<float>(a.N);
+        const float r = 1.0f / sqrtf(ms + a.eps);
+
+        if (!aborted) {
+            if (tid == 0 && crank == 0) a.rstd_out[row] = r;
+            char* yrow = ysl + static_cast<size_t>(row) * row_bytes;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int idx = v * nt + tid;
+                if (idx < nvec) {
+                    float f[VEC], w[VEC], o[VEC];
+                    E::unpack(xv[v], f);
+                    E::unpack(g[v], w);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        if (OFFSET) {
+                            const float gw = 1.0f + w[e];
+                            o[e] = (gw * f[e]) * r;
+                        } else {
+                            o[e] = (f[e] * r) * w[e];
+                        }
+                    }
+                    stg128(yrow + idx * 16, E::pack(o));
+                }
+            }
+        }
+    }
+    if (csize > 1) cluster_sync();  // no CTA leaves while a peer may read its shared memory
+    if (aborted && tid == 0) {
+        // copies issued for rows abort_row .. abort_row+S-1 may still be in flight
+        const int64_t end = abort_row + S < nrows ? abort_row + S : nrows;
+        for (int64_t j = abort_row; j < end; ++j)
+            mbar_wait_bounded(smem_u32(&full[j % S]), static_cast<uint32_t>((j / S) & 1), a.err, 1u << 16);
+    }
+}
+
+template <int DT, int EPT, bool OFFSET>
+__global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const int N = a.N;
+
+    float gv[EPT];
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        const int col = tid + k * nt;
+        float w = col < N ? E::ld(a.gamma, col) : 0.f;
+        gv[k] = OFFSET ? 1.0f + w : w;
+    }
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
+        const int64_t base = row * static_cast<int64_t>(N);
+        float xv[EPT];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int col = tid + k * nt;
+            xv[k] = col < N ? E::ld(a.x, base + col) : 0.f;
+            ss = fmaf(xv[k], xv[k], ss);
+        }
+        ss = warp_allsum(ss);
+        if (lane == 0) red[parity][warp] = ss;
+        __syncthreads();
+        float t = lane < nwarps ? red[parity][lane] : 0.f;
+        t = warp_allsum(t);
+        const float r = 1.0f / sqrtf(t / static_cast<float>(N) + a.eps);
+        if (tid == 0) a.rstd_out[row] = r;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int col = tid + k * nt;
+            if (col < N) E::st(a.y, base + col, OFFSET ? (gv[k] * xv[k]) * r : (xv[k] * r) * gv[k]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+template <int DT, bool OFF>
+static const void* fwd_tma_for(int vpt) {
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 4, OFF>);
+    case 8: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 8, OFF>);
+    default: return nullptr;
+    }
+}
+template <int DT, bool OFF>
+static const void* fwd_scalar_for(int ept) {
+    switch (ept) {
+    case 1: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 4, OFF>);
+    case 8: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 8, OFF>);
+    case 16: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 16, OFF>);
+    case 32: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 32, OFF>);
+    default: return nullptr;
+    }
+}
+template <bool OFF>
+static const void* fwd_pick(const Plan& p) {
+    const bool tma = p.path == kPathTma;
+    switch (p.dtype) {
+    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread) : fwd_scalar_for<kF32, OFF>(p.per_thread);
+    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread) : fwd_scalar_for<kF16, OFF>(p.per_thread);
+    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread) : fwd_scalar_for<kBF16, OFF>(p.per_thread);
+    default: return nullptr;
+    }
+}
+
+const void* fwd_kernel(const Plan& p) { return p.offset ? fwd_pick<true>(p) : fwd_pick<false>(p); }
+
+cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
+    const void* k = fwd_kernel(p);
+    if (!k) return cudaErrorInvalidDeviceFunction;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    RowArgs args = a;
+    void* params[] = {&args};
+    return cudaLaunchKernelExC(&cfg, k, params);
+}
+
+}  // namespace rmsnorm

@@ -1,0 +1,60 @@
+// launch.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units (fwd.cu, bwd.cu). Internal: not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rmsnorm {
+
+// Arguments of every row kernel (forward and backward use disjoint subsets).
+struct RowArgs {
+    const void* x;
+    const void* gamma;
+    const void* dy;
+    const float* rstd_in;  // backward: saved r per row
+    void* y;               // forward output
+    float* rstd_out;       // forward output
+    void* dx;              // backward output
+    float* ws;             // backward: dgamma partials [units][N]
+    int64_t M;
+    int N;
+    float eps;
+    int stages;            // TMA pipeline depth
+    uint32_t* err;         // device error word
+};
+
+enum PathKind : int { kPathTma = 0, kPathScalar = 1 };
+
+// Thread caps (also the kernels' __launch_bounds__): a TMA-path slice is at most
+// 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path holds up
+// to 32 elements per thread, so 512 threads cover N = 16384.
+constexpr int kTmaMaxThreads = 256;
+constexpr int kScalarMaxThreads = 512;
+constexpr int kScalarMaxPerThread = 32;
+
+// A launch shape chosen by the planner.
+struct Plan {
+    int path = kPathTma;
+    int dtype = 0;
+    int offset = 0;
+    int cluster = 1;       // CTAs per cluster (TMA path)
+    int threads = 0;       // threads per CTA
+    int per_thread = 0;    // TMA: 16-byte vectors per thread; scalar: elements per thread
+    int stages = 0;        // TMA pipeline depth
+    size_t smem = 0;       // dynamic shared memory per CTA
+    int64_t units = 0;     // clusters (TMA) or CTAs (scalar) = rows of dgamma partials
+};
+
+// Kernel entry for a plan (used for occupancy queries and attributes).
+const void* fwd_kernel(const Plan& p);
+const void* bwd_kernel(const Plan& p);
+const void* dgamma_reduce_kernel_ptr(int dtype);
+
+cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);
+cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s);
+cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
+                                 cudaStream_t s);
+
+}  // namespace rmsnorm

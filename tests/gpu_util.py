@@ -1,0 +1,91 @@
+"""GPU-side helpers for the tests: run the C ABI on numpy storage arrays.
+
+Output buffers carry guard regions filled with a sentinel before and after the
+data; every run checks the guards afterwards (out-of-bounds writes would show
+there). Inputs can be placed one element off a 16-byte boundary to force the
+general (scalar) path.
+"""
+import numpy as np
+
+from rmsnorm_fwd_bwd_gb300 import binding as B
+
+GUARD = 64            # elements of guard before and after each output
+SENTINEL = {"float32": np.float32(-12345.5).view(np.uint32), "float16": 0x7BFF, "bfloat16": 0x7F7F}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _guarded(n, dtype, device="cuda"):
+    """Flat buffer [GUARD + n + GUARD] filled with the sentinel; returns (buffer, view of the n)."""
+    torch = _torch()
+    if dtype == "float32":
+        buf = torch.full((n + 2 * GUARD,), float(np.uint32(SENTINEL[dtype]).view(np.float32)),
+                         dtype=torch.float32, device=device)
+    else:
+        buf = torch.full((n + 2 * GUARD,), int(np.int16(np.uint16(SENTINEL[dtype]).view(np.int16))),
+                         dtype=torch.int16, device=device).view(getattr(torch, dtype))
+    return buf, buf[GUARD:GUARD + n]
+
+
+def _guards_intact(buf, dtype):
+    a = B.to_numpy(buf, dtype)
+    if dtype == "float32":
+        a = a.view(np.uint32)
+    s = SENTINEL[dtype]
+    return bool(np.all(a[:GUARD] == s) and np.all(a[-GUARD:] == s))
+
+
+def _place(arr, dtype, misalign):
+    torch = _torch()
+    t = B.to_device(arr.reshape(-1), dtype)
+    if not misalign:
+        return t, t
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    buf[1:] = t
+    return buf, buf[1:]
+
+
+def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, stream=None):
+    """Forward (and backward) through the C ABI. Returns numpy storage arrays
+    (y, rstd, dx, dgamma); dx/dgamma are None when do_bwd is False."""
+    torch = _torch()
+    M, N = x.shape
+    keep = []
+    _, xt = _place(x, dtype, misalign); keep.append(_)
+    _, gt = _place(g, dtype, misalign); keep.append(_)
+    _, dyt = _place(dy, dtype, misalign); keep.append(_)
+    ybuf, y = _guarded(M * N, dtype)
+    rbuf, rstd = _guarded(M, "float32")
+    if misalign:
+        ybuf2 = torch.empty(M * N + 2 * GUARD + 1, dtype=y.dtype, device=y.device)
+        ybuf2[1:] = ybuf
+        ybuf, y = ybuf2[1:], ybuf2[1 + GUARD:1 + GUARD + M * N]
+    st = B.rmsnorm_fwd(xt, gt, y, rstd, M, N, eps, dtype, int(offset), stream)
+    assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+    dx = dg = None
+    dxbuf = dgbuf = None
+    if do_bwd:
+        dxbuf, dxt = _guarded(M * N, dtype)
+        dgbuf, dgt = _guarded(N, dtype)
+        if misalign:
+            b2 = torch.empty(M * N + 2 * GUARD + 1, dtype=dxt.dtype, device=dxt.device)
+            b2[1:] = dxbuf
+            dxbuf, dxt = b2[1:], b2[1 + GUARD:1 + GUARD + M * N]
+        wsz = B.rmsnorm_bwd_workspace_size(M, N, dtype)
+        ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device="cuda")
+        st = B.rmsnorm_bwd(dyt, xt, gt, rstd, dxt, dgt, M, N, dtype, int(offset), ws, wsz, stream)
+        assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+    torch.cuda.synchronize()
+    assert _guards_intact(ybuf, dtype), "forward wrote outside y"
+    assert _guards_intact(rbuf, "float32"), "forward wrote outside rstd"
+    yo = B.to_numpy(y, dtype).reshape(M, N)
+    ro = B.to_numpy(rstd, "float32")
+    if do_bwd:
+        assert _guards_intact(dxbuf, dtype), "backward wrote outside dx"
+        assert _guards_intact(dgbuf, dtype), "backward wrote outside dgamma"
+        dx = B.to_numpy(dxt, dtype).reshape(M, N)
+        dg = B.to_numpy(dgt, dtype)
+    return yo, ro, dx, dg

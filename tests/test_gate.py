@@ -115,3 +115,22 @@ def test_report_table_lists_every_tensor():
           gate.check("rstd", c["rg"], c["rr"], c["rr"], "float32")]
     text = gate.report("case", rs)
     assert "| y |" in text and "| rstd |" in text and "Overall: PASS" in text
+
+
+def test_fp32_bound_when_reference_cannot_meet_it():
+    # N = 1: dx = r*u*eps/(x^2+eps) cancels; the fp32 reference misses 1e-5 itself.
+    x, g, dy = inputs.make_inputs(37, 1, "float32", seed=1)
+    dxg, _ = orc.bwd_golden(dy, x, g, "float32")
+    dxr, _ = orc.bwd_reference(dy, x, g, "float32")
+    dxr = orc.decode(dxr, "float32")
+    assert np.max(np.abs(dxr - dxg)) / np.max(np.abs(dxg)) > gate.FP32_MAX_RELATIVE_ERROR
+    res = gate.check("dx", dxg, dxr, dxr, "float32", rel_bound=gate.FP32_MAX_RELATIVE_ERROR)
+    assert res.verdict == "PASS WITH LIMITATIONS"
+    # a target well outside the reference's envelope still fails
+    res = gate.check("dx", dxg, dxr, dxg * 1.01, "float32", rel_bound=gate.FP32_MAX_RELATIVE_ERROR)
+    assert res.verdict == "FAIL"
+    # and on a well-conditioned tensor the bound is enforced
+    c = _case("float32")
+    res = gate.check("y", c["yg"], c["yr"], c["yg"] * (1 + 3e-5), "float32",
+                     rel_bound=gate.FP32_MAX_RELATIVE_ERROR)
+    assert res.verdict == "FAIL"
