@@ -404,9 +404,14 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override the row count M (small cases for profiler captures)")
     args = ap.parse_args(argv)
+    import dataclasses
     from rmsnorm_fwd_bwd_gb300 import inputs
     w = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    if args.rows is not None:
+        w = dataclasses.replace(w, M=args.rows, name=f"{w.name}@rows={args.rows}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
