@@ -113,6 +113,34 @@ rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                            void* workspace, size_t workspace_bytes,
                            rmsnorm_stream_t stream);
 
+/*
+ * Backward without any caller-provided or library-allocated device memory.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot call cudaMalloc, for example a plugin whose host framework owns
+ * all device memory and forbids allocation, or a process that has handed the
+ * free device memory to a caching allocator and must not allocate outside it.
+ *
+ * Same arguments and results as rmsnorm_bwd, minus the workspace: the dgamma
+ * partial sums go to a fixed array of RMSNORM_STATIC_SCRATCH_BYTES (16 MiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits. Shapes whose partial sums need more than that (see
+ * rmsnorm_bwd_workspace_size) are rejected with RMSNORM_ERR_WORKSPACE before
+ * anything is launched; on a 152-SM GB300 the measured workloads need at most
+ * about 10 MiB.
+ *
+ * The first call on a device looks up the array's device address (a host-side
+ * runtime query, no allocation); make that first call before any stream
+ * capture. No call allocates. All calls on a device share the one array: two
+ * calls whose kernels overlap on the GPU (for example on different streams
+ * without ordering between them) race on it and give wrong dgamma. The array
+ * keeps the last call's partial sums; nothing in it has to start at zero.
+ */
+#define RMSNORM_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+rmsnorm_status rmsnorm_bwd_static_scratch(const void* dy, const void* x, const void* gamma,
+                                          const float* rstd, void* dx, void* dgamma,
+                                          int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
+                                          rmsnorm_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 const char* rmsnorm_status_string(rmsnorm_status status);
 

@@ -63,6 +63,7 @@ def _load():
             "rmsnorm_device_error": (I, [U32P, I]),
             "rmsnorm_describe_plan": (I, [I, I64, I64, I, I, ctypes.c_char_p, SZ]),
             "rmsnorm_set_launch_override": (I, [I, I, I, I, I]),
+            "rmsnorm_bwd_static_scratch": (I, [P, P, P, P, P, P, I64, I64, I, I, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -124,6 +125,15 @@ def rmsnorm_bwd(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, offset, workspace, 
     return _load().rmsnorm_bwd(_addr(dy), _addr(x), _addr(gamma), _addr(rstd), _addr(dx),
                                _addr(dgamma), int(M), int(N), _dtype_code(dtype), int(offset),
                                _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def rmsnorm_bwd_static_scratch(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, offset,
+                               stream=None) -> int:
+    """rmsnorm_bwd without a workspace argument: for callers that cannot allocate
+    device memory (the partial sums live in a fixed array inside the library)."""
+    return _load().rmsnorm_bwd_static_scratch(_addr(dy), _addr(x), _addr(gamma), _addr(rstd),
+                                              _addr(dx), _addr(dgamma), int(M), int(N),
+                                              _dtype_code(dtype), int(offset), _stream(stream))
 
 
 def rmsnorm_status_string(status: int) -> str:
