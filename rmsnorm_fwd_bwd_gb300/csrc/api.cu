@@ -25,9 +25,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per tensor
-constexpr int kRingBudgetBytes = 65536;  // default TMA ring size per CTA
-constexpr int kMaxStages = 8;
-constexpr int kDefaultThreadCap = 256;
+// Default ring: 2 stages, at most 3 resident blocks per SM. Measured on GB300
+// (bf16, N = 4096): deeper rings and more blocks put more requests in flight
+// and lower HBM throughput; 2 x 3 reaches the TMA-copy ceiling.
+constexpr int kDefaultStages = 2;
+constexpr int kDefaultBlocksPerSm = 3;
+constexpr int kDefaultThreadCap[2] = {256, 128};  // forward, backward
 
 struct DeviceInfo {
     bool ready = false;
@@ -129,7 +132,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : kDefaultThreadCap;
+        const int cap = ov.threads ? ov.threads : kDefaultThreadCap[pass];
         for (vpt = 1; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
@@ -142,10 +145,9 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     if ((threads / 32) * cl > 32) return false;
     const int slice = (N / cl) * s;
     const int stage = (pass == 0 ? 1 : 2) * slice;
-    const int fixed = 2 * 32 * 4 + 16;
-    int stages = ov.stages ? ov.stages : kRingBudgetBytes / stage;
-    if (stages > kMaxStages && !ov.stages) stages = kMaxStages;
-    if (stages < 2) stages = 2;
+    // warp partials, abort flag (+ the backward's fp32 gamma slice)
+    const int fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : (N / cl) * 4);
+    int stages = ov.stages ? ov.stages : kDefaultStages;
     while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
     if (stages < 1) return false;
     p.path = kPathTma;
@@ -159,7 +161,8 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
-    if (!occupancy_units(k, p, di, ov.blocks_per_sm, units)) return false;
+    if (!occupancy_units(k, p, di, ov.blocks_per_sm ? ov.blocks_per_sm : kDefaultBlocksPerSm, units))
+        return false;
     p.units = units < M ? units : M;
     return true;
 }

@@ -1,7 +1,7 @@
 // bwd.cu -- RMSNorm backward kernels.
 //
 // Per row, with r the saved forward value and g = gamma (or 1 + w):
-//     u = dy * g;   c = sum_j(u_j * x_j) / N;   dx = (r * u) - ((x * r^3) * c)
+//     u = dy * g;   c = sum_j(u_j * x_j) / N;   dx = r * u - x * r^3 * c
 // and, per column, dgamma_j = sum over rows of (dy_j * x_j) * r
 // (page "Check an AI model calculation before accelerating it", sections
 // "Input backward pass: keep the right N", "Where does the cube of r come
@@ -21,7 +21,7 @@
 
 namespace rmsnorm {
 
-template <int DT, int VPT, bool OFFSET>
+template <int DT, int VPT, bool OFFSET, bool CLUSTER>
 __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
@@ -32,10 +32,10 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int nwarps = nt >> 5;
-    const uint32_t crank = cluster_rank();
-    const uint32_t csize = cluster_size();
-    const int64_t cid = cluster_id();
-    const int64_t ncl = cluster_count();
+    const uint32_t crank = CLUSTER ? cluster_rank() : 0u;
+    const uint32_t csize = CLUSTER ? cluster_size() : 1u;
+    const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t ncl = CLUSTER ? static_cast<int64_t>(cluster_count()) : static_cast<int64_t>(gridDim.x);
 
     const int ns = a.N / static_cast<int>(csize);
     const int nvec = ns / VEC;
@@ -44,9 +44,12 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
     const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
     const int S = a.stages;
 
+    // shared memory: ring | gamma slice in fp32 | mbarriers | warp partials [2][32] | abort flag
     unsigned char* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
+    float* gsm = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(gsm + ns);
     float* red = reinterpret_cast<float*>(full + S);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
 
     const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
     const size_t slice_off = static_cast<size_t>(crank) * slice_bytes;
@@ -54,13 +57,18 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
     const char* dysl = static_cast<const char*>(a.dy) + slice_off;
     char* dxsl = static_cast<char*>(a.dx) + slice_off;
 
-    uint4 g[VPT];
+    // gamma slice widened once (offset variant: 1 + w) into shared memory
     {
         const uint4* gs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.gamma) + slice_off);
+        for (int idx = tid; idx < nvec; idx += nt) {
+            float w[VEC];
+            E::unpack(__ldg(gs + idx), w);
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int idx = v * nt + tid;
-            g[v] = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < VEC; q += 4) {
+                float4 f = OFFSET ? make_float4(1.0f + w[q], 1.0f + w[q + 1], 1.0f + w[q + 2], 1.0f + w[q + 3])
+                                  : make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+                *reinterpret_cast<float4*>(gsm + idx * VEC + q) = f;
+            }
         }
     }
     float acc[VPT][VEC];
@@ -71,10 +79,11 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (csize > 1) cluster_sync();
+    if (CLUSTER) cluster_sync();
 
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
@@ -88,66 +97,81 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
         for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stage_bytes, smem_u32(&full[j]));
     }
 
-    float r_next = nrows > 0 ? __ldg(a.rstd_in + cid) : 0.f;
+    // saved r, 32 rows per warp-wide load, fetched 32 rows ahead of use
+    auto rstd_at = [&](int64_t jj) -> float {
+        return jj < nrows ? __ldg(a.rstd_in + cid + jj * ncl) : 0.f;
+    };
+    float r_cur = rstd_at(lane);
+    float r_next = rstd_at(32 + lane);
+
     bool aborted = false;
     int64_t abort_row = nrows;
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t j = 0; j < nrows; ++j) {
-        const int s = static_cast<int>(j % S);
-        const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
         const int64_t row = cid + j * ncl;
         const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
-        const float r = r_next;
-        if (j + 1 < nrows) r_next = __ldg(a.rstd_in + row + ncl);
+        if ((j & 31) == 0 && j > 0) {
+            r_cur = r_next;
+            r_next = rstd_at(j + 32 + lane);
+        }
+        const float r = __shfl_sync(0xffffffffu, r_cur, static_cast<int>(j & 31));
 
-        bool ok = true;
-        if (!aborted) ok = mbar_wait_bounded(smem_u32(&full[s]), parity, a.err);
+        if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        uint4 xv[VPT], dv[VPT];
+        float xf[VPT][VEC], uf[VPT][VEC];
         float p0 = 0.f, p1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
+            float df[VEC], g[VEC];
             if (idx < nvec) {
-                xv[v] = *reinterpret_cast<const uint4*>(st + idx * 16);
-                dv[v] = *reinterpret_cast<const uint4*>(st + slice_bytes + idx * 16);
+                E::unpack(*reinterpret_cast<const uint4*>(st + idx * 16), xf[v]);
+                E::unpack(*reinterpret_cast<const uint4*>(st + slice_bytes + idx * 16), df);
+#pragma unroll
+                for (int q = 0; q < VEC; q += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(gsm + idx * VEC + q);
+                    g[q] = f.x; g[q + 1] = f.y; g[q + 2] = f.z; g[q + 3] = f.w;
+                }
             } else {
-                xv[v] = make_uint4(0, 0, 0, 0);
-                dv[v] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) xf[v][e] = df[e] = g[e] = 0.f;
             }
-            float xf[VEC], df[VEC], w[VEC];
-            E::unpack(xv[v], xf);
-            E::unpack(dv[v], df);
-            E::unpack(g[v], w);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                const float gw = OFFSET ? 1.0f + w[e] : w[e];
-                const float u = __fmul_rn(df[e], gw);
-                if (e & 1) p1 = fmaf(u, xf[e], p1); else p0 = fmaf(u, xf[e], p0);
-                acc[v][e] = fmaf(__fmul_rn(df[e], xf[e]), r, acc[v][e]);
+                uf[v][e] = __fmul_rn(df[e], g[e]);
+                if (e & 1) p1 = fmaf(uf[v][e], xf[v][e], p1); else p0 = fmaf(uf[v][e], xf[v][e], p0);
+                acc[v][e] = fmaf(__fmul_rn(df[e], xf[v][e]), r, acc[v][e]);
             }
         }
         float* redb = red + (j & 1) * 32;
         const float wsum = warp_allsum(p0 + p1);
         if (lane == 0) redb[warp] = wsum;
-        const bool now_aborted = __syncthreads_or(aborted || !ok) != 0;
-        if (now_aborted && !aborted) abort_row = j;
-        aborted = now_aborted;
-        if (csize > 1) cluster_sync();
+        if (CLUSTER) cluster_sync(); else __syncthreads();
+        if (!aborted && *abort_flag) {
+            aborted = true;
+            abort_row = j;
+        }
 
         if (tid == 0 && !aborted && j + S < nrows) {
             fence_proxy_async_smem();
             issue(j + S, st, smem_u32(&full[s]));
         }
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
 
         float t = 0.f;
-        if (csize == 1) {
+        if (!CLUSTER) {
             if (lane < nwarps) t = redb[lane];
         } else if (lane < nwarps * static_cast<int>(csize)) {
             t = dsmem_ld_f32(dsmem_map(smem_u32(redb + lane % nwarps), lane / nwarps));
         }
         t = warp_allsum(t);
         const float c = t / static_cast<float>(a.N);
-        const float r3 = __fmul_rn(__fmul_rn(r, r), r);
+        // dx = r*u - x*k with k = r^3 * c, as one fused multiply-add per element
+        const float k = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), c);
 
         if (!aborted) {
             char* dxrow = dxsl + static_cast<size_t>(row) * row_bytes;
@@ -155,16 +179,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
             for (int v = 0; v < VPT; ++v) {
                 const int idx = v * nt + tid;
                 if (idx < nvec) {
-                    float xf[VEC], df[VEC], w[VEC], o[VEC];
-                    E::unpack(xv[v], xf);
-                    E::unpack(dv[v], df);
-                    E::unpack(g[v], w);
+                    float o[VEC];
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float gw = OFFSET ? 1.0f + w[e] : w[e];
-                        const float u = __fmul_rn(df[e], gw);
-                        o[e] = __fsub_rn(__fmul_rn(r, u), __fmul_rn(__fmul_rn(xf[e], r3), c));
-                    }
+                    for (int e = 0; e < VEC; ++e) o[e] = fmaf(-xf[v][e], k, __fmul_rn(r, uf[v][e]));
                     stg128(dxrow + idx * 16, E::pack(o));
                 }
             }
@@ -185,7 +202,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
             }
         }
     }
-    if (csize > 1) cluster_sync();
+    if (CLUSTER) cluster_sync();
     if (aborted && tid == 0) {
         const int64_t end = abort_row + S < nrows ? abort_row + S : nrows;
         for (int64_t j = abort_row; j < end; ++j)
@@ -289,15 +306,19 @@ __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
-template <int DT, bool OFF>
-static const void* bwd_tma_for(int vpt) {
+template <int DT, bool OFF, bool CL>
+static const void* bwd_tma_vpt(int vpt) {
     switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 1, OFF>);
-    case 2: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 2, OFF>);
-    case 4: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 4, OFF>);
-    case 8: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 8, OFF>);
+    case 1: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 1, OFF, CL>);
+    case 2: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 2, OFF, CL>);
+    case 4: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 4, OFF, CL>);
+    case 8: return reinterpret_cast<const void*>(&bwd_tma_kernel<DT, 8, OFF, CL>);
     default: return nullptr;
     }
+}
+template <int DT, bool OFF>
+static const void* bwd_tma_for(int vpt, int cluster) {
+    return cluster > 1 ? bwd_tma_vpt<DT, OFF, true>(vpt) : bwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
 static const void* bwd_scalar_for(int ept) {
@@ -315,9 +336,9 @@ template <bool OFF>
 static const void* bwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
     switch (p.dtype) {
-    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread) : bwd_scalar_for<kF32, OFF>(p.per_thread);
-    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread) : bwd_scalar_for<kF16, OFF>(p.per_thread);
-    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread) : bwd_scalar_for<kBF16, OFF>(p.per_thread);
+    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF32, OFF>(p.per_thread);
+    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF16, OFF>(p.per_thread);
+    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kBF16, OFF>(p.per_thread);
     default: return nullptr;
     }
 }

@@ -25,7 +25,7 @@
 
 namespace rmsnorm {
 
-template <int DT, int VPT, bool OFFSET>
+template <int DT, int VPT, bool OFFSET, bool CLUSTER>
 __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
@@ -36,10 +36,10 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int nwarps = nt >> 5;
-    const uint32_t crank = cluster_rank();
-    const uint32_t csize = cluster_size();
-    const int64_t cid = cluster_id();
-    const int64_t ncl = cluster_count();
+    const uint32_t crank = CLUSTER ? cluster_rank() : 0u;
+    const uint32_t csize = CLUSTER ? cluster_size() : 1u;
+    const int64_t cid = CLUSTER ? static_cast<int64_t>(cluster_id()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t ncl = CLUSTER ? static_cast<int64_t>(cluster_count()) : static_cast<int64_t>(gridDim.x);
 
     const int ns = a.N / static_cast<int>(csize);  // slice width (elements)
     const int nvec = ns / VEC;                       // 16-byte vectors per slice
@@ -47,32 +47,39 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
     const int S = a.stages;
 
+    // shared memory: ring | mbarriers | warp partials [2][32] | abort flag
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * slice_bytes);
-    float* red = reinterpret_cast<float*>(full + S);  // [2][32] warp partials
+    float* red = reinterpret_cast<float*>(full + S);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
 
     const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
     const char* xsl = static_cast<const char*>(a.x) + static_cast<size_t>(crank) * slice_bytes;
     char* ysl = static_cast<char*>(a.y) + static_cast<size_t>(crank) * slice_bytes;
 
-    // gamma slice, raw, in registers for the whole kernel
-    uint4 g[VPT];
+    // gamma slice widened to fp32 once (offset variant: 1 + w), kept in registers
+    float gf[VPT][VEC];
     {
         const uint4* gs = reinterpret_cast<const uint4*>(
             static_cast<const char*>(a.gamma) + static_cast<size_t>(crank) * slice_bytes);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
-            g[v] = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+            E::unpack(idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0), gf[v]);
+            if (OFFSET) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) gf[v][e] = 1.0f + gf[v][e];
+            }
         }
     }
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (csize > 1) cluster_sync();  // peers' shared memory is live before any DSMEM read
+    if (CLUSTER) cluster_sync();  // peers' shared memory is live before any DSMEM read
 
     const uint64_t pol = l2_evict_first_policy();
     if (tid == 0) {
@@ -87,37 +94,37 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
 
     bool aborted = false;
     int64_t abort_row = nrows;
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t j = 0; j < nrows; ++j) {
-        const int s = static_cast<int>(j % S);
-        const uint32_t parity = static_cast<uint32_t>((j / S) & 1);
         const int64_t row = cid + j * ncl;
         const unsigned char* st = ring + static_cast<size_t>(s) * slice_bytes;
 
-        bool ok = true;
-        if (!aborted) ok = mbar_wait_bounded(smem_u32(&full[s]), parity, a.err);
+        if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        uint4 xv[VPT];
+        // x slice widened to fp32 once; sum of squares on the way
+        float xf[VPT][VEC];
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
-            xv[v] = idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0);
-            float f[VEC];
-            E::unpack(xv[v], f);
+            E::unpack(idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0),
+                      xf[v]);
 #pragma unroll
             for (int e = 0; e < VEC; e += 2) {
-                ss0 = fmaf(f[e], f[e], ss0);
-                ss1 = fmaf(f[e + 1], f[e + 1], ss1);
+                ss0 = fmaf(xf[v][e], xf[v][e], ss0);
+                ss1 = fmaf(xf[v][e + 1], xf[v][e + 1], ss1);
             }
         }
         float* redb = red + (j & 1) * 32;
         const float wsum = warp_allsum(ss0 + ss1);
         if (lane == 0) redb[warp] = wsum;
         // every thread has its slice in registers after this barrier: the stage can refill
-        const bool now_aborted = __syncthreads_or(aborted || !ok) != 0;
-        if (now_aborted && !aborted) abort_row = j;
-        aborted = now_aborted;
-        if (csize > 1) cluster_sync();
+        if (CLUSTER) cluster_sync(); else __syncthreads();
+        if (!aborted && *abort_flag) {
+            aborted = true;
+            abort_row = j;
+        }
 
         if (tid == 0 && !aborted && j + S < nrows) {
             fence_proxy_async_smem();
@@ -125,9 +132,13 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
             mbar_arrive_expect_tx(bar, slice_bytes);
             bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * row_bytes, slice_bytes, bar, pol);
         }
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
 
         float t = 0.f;
-        if (csize == 1) {
+        if (!CLUSTER) {
             if (lane < nwarps) t = redb[lane];
         } else if (lane < nwarps * static_cast<int>(csize)) {
             t = dsmem_ld_f32(dsmem_map(smem_u32(redb + lane % nwarps), lane / nwarps));
@@ -143,24 +154,16 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
             for (int v = 0; v < VPT; ++v) {
                 const int idx = v * nt + tid;
                 if (idx < nvec) {
-                    float f[VEC], w[VEC], o[VEC];
-                    E::unpack(xv[v], f);
-                    E::unpack(g[v], w);
+                    float o[VEC];
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        if (OFFSET) {
-                            const float gw = 1.0f + w[e];
-                            o[e] = (gw * f[e]) * r;
-                        } else {
-                            o[e] = (f[e] * r) * w[e];
-                        }
-                    }
+                    for (int e = 0; e < VEC; ++e)
+                        o[e] = OFFSET ? (gf[v][e] * xf[v][e]) * r : (xf[v][e] * r) * gf[v][e];
                     stg128(yrow + idx * 16, E::pack(o));
                 }
             }
         }
     }
-    if (csize > 1) cluster_sync();  // no CTA leaves while a peer may read its shared memory
+    if (CLUSTER) cluster_sync();  // no CTA leaves while a peer may read its shared memory
     if (aborted && tid == 0) {
         // copies issued for rows abort_row .. abort_row+S-1 may still be in flight
         const int64_t end = abort_row + S < nrows ? abort_row + S : nrows;
@@ -216,15 +219,19 @@ __global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const Row
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
-template <int DT, bool OFF>
-static const void* fwd_tma_for(int vpt) {
+template <int DT, bool OFF, bool CL>
+static const void* fwd_tma_vpt(int vpt) {
     switch (vpt) {
-    case 1: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 1, OFF>);
-    case 2: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 2, OFF>);
-    case 4: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 4, OFF>);
-    case 8: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 8, OFF>);
+    case 1: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 1, OFF, CL>);
+    case 2: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 2, OFF, CL>);
+    case 4: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 4, OFF, CL>);
+    case 8: return reinterpret_cast<const void*>(&fwd_tma_kernel<DT, 8, OFF, CL>);
     default: return nullptr;
     }
+}
+template <int DT, bool OFF>
+static const void* fwd_tma_for(int vpt, int cluster) {
+    return cluster > 1 ? fwd_tma_vpt<DT, OFF, true>(vpt) : fwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
 static const void* fwd_scalar_for(int ept) {
@@ -242,9 +249,9 @@ template <bool OFF>
 static const void* fwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
     switch (p.dtype) {
-    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread) : fwd_scalar_for<kF32, OFF>(p.per_thread);
-    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread) : fwd_scalar_for<kF16, OFF>(p.per_thread);
-    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread) : fwd_scalar_for<kBF16, OFF>(p.per_thread);
+    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF32, OFF>(p.per_thread);
+    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF16, OFF>(p.per_thread);
+    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kBF16, OFF>(p.per_thread);
     default: return nullptr;
     }
 }
