@@ -57,7 +57,16 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
     const char* dysl = static_cast<const char*>(a.dy) + slice_off;
     char* dxsl = static_cast<char*>(a.dx) + slice_off;
 
-    // gamma slice widened once (offset variant: 1 + w) into shared memory
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+
+    // gamma slice widened once (offset variant: 1 + w) into shared memory, as
+    // VEC/4 planes of float4 so that a warp reads 512 consecutive bytes per plane
+    float4* gsm4 = reinterpret_cast<float4*>(gsm);
     {
         const uint4* gs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.gamma) + slice_off);
         for (int idx = tid; idx < nvec; idx += nt) {
@@ -67,7 +76,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
             for (int q = 0; q < VEC; q += 4) {
                 float4 f = OFFSET ? make_float4(1.0f + w[q], 1.0f + w[q + 1], 1.0f + w[q + 2], 1.0f + w[q + 3])
                                   : make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
-                *reinterpret_cast<float4*>(gsm + idx * VEC + q) = f;
+                gsm4[(q / 4) * nvec + idx] = f;
             }
         }
     }
@@ -77,11 +86,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
     __syncthreads();
     if (CLUSTER) cluster_sync();
 
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
                 E::unpack(*reinterpret_cast<const uint4*>(st + slice_bytes + idx * 16), df);
 #pragma unroll
                 for (int q = 0; q < VEC; q += 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(gsm + idx * VEC + q);
+                    const float4 f = gsm4[(q / 4) * nvec + idx];
                     g[q] = f.x; g[q + 1] = f.y; g[q + 2] = f.z; g[q + 3] = f.w;
                 }
             } else {
@@ -188,6 +192,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
         }
     }
 
+    griddep_launch_dependents();
     // one row of dgamma partials per cluster: ws[cid][crank*ns + ...]
     if (!aborted) {
         float* wrow = a.ws + static_cast<size_t>(cid) * a.N + static_cast<size_t>(crank) * ns;
@@ -225,6 +230,7 @@ __global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const Row
     const int warp = tid >> 5;
     const int nwarps = nt >> 5;
     const int N = a.N;
+    griddep_wait();
 
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const Row
             }
         }
     }
+    griddep_launch_dependents();
     if (blockIdx.x < a.M) {
         float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
 #pragma unroll
@@ -279,27 +286,51 @@ __global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const Row
     }
 }
 
-// dgamma[j] = sum_{p < units} ws[p][j], fixed order: thread (tx, ty) sums rows
-// ty, ty+8, ... of column j in sequence, then the 8 partial sums are added in a
-// fixed tree. units == 0 (no rows) writes zeros.
+// dgamma[j] = sum_{p < units} ws[p][j] in a fixed order. A block owns 32
+// columns; thread (cq, ry) owns columns 4cq..4cq+3 of them and sums rows
+// ry, ry + 32, ... in sequence (8 threads read 128 contiguous bytes of a row);
+// then thread cq adds the 32 row-lane sums in ry order. units == 0 (no rows)
+// writes zeros. Rows of N % 4 != 0 floats are read one column at a time.
 template <int DT>
 __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
                                                            void* dgamma) {
     using E = Elem<DT>;
-    __shared__ float part[8][33];
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int col = blockIdx.x * 32 + tx;
-    float s = 0.f;
-    if (col < N) {
+    __shared__ float4 part[32][8];
+    const int cq = threadIdx.x & 7;
+    const int ry = threadIdx.x >> 3;
+    const int col = blockIdx.x * 32 + cq * 4;
+    griddep_wait();  // the partial sums come from the row kernel just before
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if ((N & 3) == 0) {
+        if (col < N) {
 #pragma unroll 4
-        for (int64_t p = ty; p < units; p += 8) s += ws[p * N + col];
+            for (int64_t p = ry; p < units; p += 32) {
+                const float4 v = *reinterpret_cast<const float4*>(ws + p * N + col);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
+        }
+    } else {
+#pragma unroll 2
+        for (int64_t p = ry; p < units; p += 32) {
+            const float* rowp = ws + p * N;
+            if (col < N) s.x += rowp[col];
+            if (col + 1 < N) s.y += rowp[col + 1];
+            if (col + 2 < N) s.z += rowp[col + 2];
+            if (col + 3 < N) s.w += rowp[col + 3];
+        }
     }
-    part[ty][tx] = s;
+    part[ry][cq] = s;
     __syncthreads();
-    if (ty == 0 && col < N) {
-        const float t = ((part[0][tx] + part[1][tx]) + (part[2][tx] + part[3][tx])) +
-                        ((part[4][tx] + part[5][tx]) + (part[6][tx] + part[7][tx]));
-        E::st(dgamma, col, t);
+    if (ry == 0) {
+        float4 t = part[0][cq];
+        for (int k = 1; k < 32; ++k) {
+            const float4 v = part[k][cq];
+            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+        }
+        if (col < N) E::st(dgamma, col, t.x);
+        if (col + 1 < N) E::st(dgamma, col + 1, t.y);
+        if (col + 2 < N) E::st(dgamma, col + 2, t.z);
+        if (col + 3 < N) E::st(dgamma, col + 3, t.w);
     }
 }
 
@@ -362,7 +393,7 @@ cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     if (p.cluster > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
@@ -371,6 +402,10 @@ cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
     RowArgs args = a;
     void* params[] = {&args};
     return cudaLaunchKernelExC(&cfg, k, params);
@@ -382,9 +417,14 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), 1, 1);
-    cfg.blockDim = dim3(32, 8, 1);
+    cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma};
     return cudaLaunchKernelExC(&cfg, k, params);
 }

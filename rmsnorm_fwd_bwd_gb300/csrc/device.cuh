@@ -219,6 +219,17 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     return v;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start before the previous kernel on the stream finishes;
+// griddep_wait() blocks until that kernel has completed and its memory is
+// visible (a no-op when the launch did not use the attribute), so it must come
+// before the first read of anything the previous kernel may have written.
+// griddep_launch_dependents() lets the next such kernel begin launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 16-byte global stores: default caching, and cache-streaming (evict-first).
 __device__ __forceinline__ void stg128(void* p, const uint4& v) {
     *reinterpret_cast<uint4*>(p) = v;

@@ -57,6 +57,13 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     const char* xsl = static_cast<const char*>(a.x) + static_cast<size_t>(crank) * slice_bytes;
     char* ysl = static_cast<char*>(a.y) + static_cast<size_t>(crank) * slice_bytes;
 
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+
     // gamma slice widened to fp32 once (offset variant: 1 + w), kept in registers
     float gf[VPT][VEC];
     {
@@ -73,11 +80,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
         }
     }
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
     __syncthreads();
     if (CLUSTER) cluster_sync();  // peers' shared memory is live before any DSMEM read
 
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
             }
         }
     }
+    griddep_launch_dependents();
     if (CLUSTER) cluster_sync();  // no CTA leaves while a peer may read its shared memory
     if (aborted && tid == 0) {
         // copies issued for rows abort_row .. abort_row+S-1 may still be in flight
@@ -182,6 +185,7 @@ __global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const Row
     const int warp = tid >> 5;
     const int nwarps = nt >> 5;
     const int N = a.N;
+    griddep_wait();
 
     float gv[EPT];
 #pragma unroll
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const Row
             if (col < N) E::st(a.y, base + col, OFFSET ? (gv[k] * xv[k]) * r : (xv[k] * r) * gv[k]);
         }
     }
+    griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -266,7 +271,7 @@ cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     if (p.cluster > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
@@ -275,6 +280,10 @@ cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
     RowArgs args = a;
     void* params[] = {&args};
     return cudaLaunchKernelExC(&cfg, k, params);
