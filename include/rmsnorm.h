@@ -153,6 +153,15 @@ const char* rmsnorm_status_string(rmsnorm_status status);
 rmsnorm_status rmsnorm_device_error(uint32_t* flags, int clear);
 
 /*
+ * Self-test of the bounded waits behind rmsnorm_device_error: launches one
+ * block on `stream` that waits, at most `polls` times (1 .. 2^21), on an
+ * mbarrier that nothing ever completes. The wait gives up, the kernel sets
+ * bit 0 of the device error word and returns; the CUDA context stays usable.
+ * A diagnostic for the failure-detection path; no counterpart on the pages.
+ */
+rmsnorm_status rmsnorm_selftest_wait_timeout(uint32_t polls, rmsnorm_stream_t stream);
+
+/*
  * Launch plan the library would use, as text (for logs and tests), e.g.
  * "tma cluster=1 threads=256 vpt=2 stages=6 blocks=456". pass: 0 = forward,
  * 1 = backward. aligned16: whether the data pointers will be 16-byte aligned.

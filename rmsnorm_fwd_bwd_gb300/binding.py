@@ -64,6 +64,7 @@ def _load():
             "rmsnorm_describe_plan": (I, [I, I64, I64, I, I, ctypes.c_char_p, SZ]),
             "rmsnorm_set_launch_override": (I, [I, I, I, I, I]),
             "rmsnorm_bwd_static_scratch": (I, [P, P, P, P, P, P, I64, I64, I, I, P]),
+            "rmsnorm_selftest_wait_timeout": (I, [ctypes.c_uint32, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -146,6 +147,10 @@ def rmsnorm_device_error(clear: bool = False) -> int:
     if st != RMSNORM_OK:
         raise RMSNormError(st, "rmsnorm_device_error")
     return int(flags.value)
+
+
+def rmsnorm_selftest_wait_timeout(polls, stream=None) -> int:
+    return _load().rmsnorm_selftest_wait_timeout(int(polls), _stream(stream))
 
 
 def rmsnorm_describe_plan(pass_, M, N, dtype, aligned16=True) -> str:

@@ -7,6 +7,7 @@
 // checked before any output is written and unsupported inputs are rejected
 // rather than routed to another implementation (section "Adapting the kernel
 // and moving to production": no silent fallback).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -31,6 +32,14 @@ constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per te
 constexpr int kDefaultStages = 2;
 constexpr int kDefaultBlocksPerSm = 3;
 constexpr int kDefaultThreadCap[2] = {256, 128};  // forward, backward
+// Rows split over a cluster pay a cluster barrier per row; measured on GB300
+// (fp16/fp32, N = 8192-16384) a third stage and more resident blocks hide it.
+constexpr int kClusterStages[2] = {3, 2};
+constexpr int kClusterBlocksPerSm[2] = {6, 3};
+constexpr int kClusterThreadCap[2] = {128, 256};
+// Bound on the general path's backward workspace; more blocks than this add
+// little once every SM holds one.
+constexpr int64_t kScalarWorkspaceCap = int64_t(8) << 20;
 
 struct DeviceInfo {
     bool ready = false;
@@ -132,7 +141,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : kDefaultThreadCap[pass];
+        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kDefaultThreadCap[pass]);
         for (vpt = 1; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
@@ -147,7 +156,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const int stage = (pass == 0 ? 1 : 2) * slice;
     // warp partials, abort flag (+ the backward's fp32 gamma slice)
     const int fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : (N / cl) * 4);
-    int stages = ov.stages ? ov.stages : kDefaultStages;
+    int stages = ov.stages ? ov.stages : (cl > 1 ? kClusterStages[pass] : kDefaultStages);
     while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
     if (stages < 1) return false;
     p.path = kPathTma;
@@ -161,30 +170,33 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
-    if (!occupancy_units(k, p, di, ov.blocks_per_sm ? ov.blocks_per_sm : kDefaultBlocksPerSm, units))
-        return false;
+    const int bps = ov.blocks_per_sm ? ov.blocks_per_sm : (cl > 1 ? kClusterBlocksPerSm[pass] : kDefaultBlocksPerSm);
+    if (!occupancy_units(k, p, di, bps, units)) return false;
     p.units = units < M ? units : M;
     return true;
 }
 
-// General path: any N (<= RMSNORM_MAX_N) and element alignment, one CTA per row.
+// General path: any N (<= RMSNORM_MAX_N) and element alignment, one CTA per row,
+// as many resident blocks as fit.
 bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
-    int ept = 1;
-    while (ept < kScalarMaxPerThread && round_up(ceil_div(N, ept), 32) > kScalarMaxThreads) ept *= 2;
-    const int threads = static_cast<int>(round_up(ceil_div(N, ept), 32));
-    if (threads > kScalarMaxThreads) return false;
+    const int threads = static_cast<int>(N >= kScalarThreads ? kScalarThreads : round_up(N, 32));
     p.path = kPathScalar;
     p.dtype = dt;
     p.offset = offset;
     p.cluster = 1;
     p.threads = threads;
-    p.per_thread = ept;
+    p.per_thread = 0;
     p.stages = 0;
     p.smem = pass == 0 ? 0 : static_cast<size_t>(N) * 4;
     const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
     if (!occupancy_units(k, p, di, 0, units)) return false;
+    if (pass == 1) {
+        // keep the dgamma partials (units x N floats) within kScalarWorkspaceCap
+        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
+        if (units > cap) units = cap;
+    }
     p.units = units < M ? units : M;
     return true;
 }
@@ -227,6 +239,18 @@ rmsnorm_status current_device(int& dev, DeviceInfo*& di) {
 }
 
 }  // namespace
+
+uint32_t* device_error_word() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (current_device(dev, di) != RMSNORM_OK) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return di->err;
+}
+
 }  // namespace rmsnorm
 
 using namespace rmsnorm;
@@ -366,7 +390,7 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
         snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.cluster,
                  p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
     else
-        snprintf(buf, buf_len, "scalar threads=%d ept=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
+        snprintf(buf, buf_len, "scalar threads=%d units=%lld smem=%zu sms=%d", p.threads,
                  static_cast<long long>(p.units), p.smem, di->sms);
     return RMSNORM_OK;
 }

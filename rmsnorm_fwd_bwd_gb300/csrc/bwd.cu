@@ -216,10 +216,11 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
 }
 
 // General path: any N, any element alignment. One CTA per row (persistent);
-// thread t owns columns t, t + nt, ...; dgamma accumulators live in shared
-// memory indexed by column (each column is touched by one thread only).
-template <int DT, int EPT, bool OFFSET>
-__global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const RowArgs a) {
+// thread t owns columns t, t + nt, ...; two passes over the row (the second is
+// served by L1/L2); dgamma accumulators live in shared memory indexed by column
+// (each column is touched by one thread only).
+template <int DT, bool OFFSET>
+__global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArgs a) {
     using E = Elem<DT>;
     extern __shared__ __align__(16) unsigned char smem[];
     float* acc = reinterpret_cast<float*>(smem);  // [N]
@@ -232,57 +233,51 @@ __global__ void __launch_bounds__(kScalarMaxThreads) bwd_scalar_kernel(const Row
     const int N = a.N;
     griddep_wait();
 
-#pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-        const int col = tid + k * nt;
-        if (col < N) acc[col] = 0.f;
-    }
+    for (int c = tid; c < N; c += nt) acc[c] = 0.f;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t base = row * static_cast<int64_t>(N);
         const float r = __ldg(a.rstd_in + row);
-        float xv[EPT], dv[EPT];
-        float p = 0.f;
-#pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int col = tid + k * nt;
-            if (col < N) {
-                xv[k] = E::ld(a.x, base + col);
-                dv[k] = E::ld(a.dy, base + col);
-                const float w = E::ld(a.gamma, col);
-                const float u = __fmul_rn(dv[k], OFFSET ? 1.0f + w : w);
-                p = fmaf(u, xv[k], p);
-                acc[col] = fmaf(__fmul_rn(dv[k], xv[k]), r, acc[col]);
-            } else {
-                xv[k] = 0.f;
-                dv[k] = 0.f;
-            }
+        // pass 1: sum of u*x, and this row's dgamma terms
+        float p0 = 0.f, p1 = 0.f;
+        int col = tid;
+        for (; col + nt < N; col += 2 * nt) {
+            const float x0 = E::ld(a.x, base + col), x1 = E::ld(a.x, base + col + nt);
+            const float d0 = E::ld(a.dy, base + col), d1 = E::ld(a.dy, base + col + nt);
+            const float w0 = E::ld(a.gamma, col), w1 = E::ld(a.gamma, col + nt);
+            p0 = fmaf(__fmul_rn(d0, OFFSET ? 1.0f + w0 : w0), x0, p0);
+            p1 = fmaf(__fmul_rn(d1, OFFSET ? 1.0f + w1 : w1), x1, p1);
+            acc[col] = fmaf(__fmul_rn(d0, x0), r, acc[col]);
+            acc[col + nt] = fmaf(__fmul_rn(d1, x1), r, acc[col + nt]);
         }
-        p = warp_allsum(p);
-        if (lane == 0) red[parity][warp] = p;
+        for (; col < N; col += nt) {
+            const float x0 = E::ld(a.x, base + col);
+            const float d0 = E::ld(a.dy, base + col);
+            const float w0 = E::ld(a.gamma, col);
+            p0 = fmaf(__fmul_rn(d0, OFFSET ? 1.0f + w0 : w0), x0, p0);
+            acc[col] = fmaf(__fmul_rn(d0, x0), r, acc[col]);
+        }
+        const float ws = warp_allsum(p0 + p1);
+        if (lane == 0) red[parity][warp] = ws;
         __syncthreads();
         float t = lane < nwarps ? red[parity][lane] : 0.f;
         t = warp_allsum(t);
         const float c = t / static_cast<float>(N);
-        const float r3 = __fmul_rn(__fmul_rn(r, r), r);
-#pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int col = tid + k * nt;
-            if (col < N) {
-                const float w = E::ld(a.gamma, col);
-                const float u = __fmul_rn(dv[k], OFFSET ? 1.0f + w : w);
-                E::st(a.dx, base + col, __fsub_rn(__fmul_rn(r, u), __fmul_rn(__fmul_rn(xv[k], r3), c)));
-            }
+        const float k = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), c);  // dx = r*u - x*k
+        // pass 2: the row again (now in L1/L2), dx
+#pragma unroll 4
+        for (int cc = tid; cc < N; cc += nt) {
+            const float xv = E::ld(a.x, base + cc);
+            const float dv = E::ld(a.dy, base + cc);
+            const float w = E::ld(a.gamma, cc);
+            const float u = __fmul_rn(dv, OFFSET ? 1.0f + w : w);
+            E::st(a.dx, base + cc, fmaf(-xv, k, __fmul_rn(r, u)));
         }
     }
     griddep_launch_dependents();
     if (blockIdx.x < a.M) {
         float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
-#pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int col = tid + k * nt;
-            if (col < N) wrow[col] = acc[col];
-        }
+        for (int c = tid; c < N; c += nt) wrow[c] = acc[c];
     }
 }
 
@@ -352,24 +347,16 @@ static const void* bwd_tma_for(int vpt, int cluster) {
     return cluster > 1 ? bwd_tma_vpt<DT, OFF, true>(vpt) : bwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
-static const void* bwd_scalar_for(int ept) {
-    switch (ept) {
-    case 1: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 1, OFF>);
-    case 2: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 2, OFF>);
-    case 4: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 4, OFF>);
-    case 8: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 8, OFF>);
-    case 16: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 16, OFF>);
-    case 32: return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, 32, OFF>);
-    default: return nullptr;
-    }
+static const void* bwd_scalar_for() {
+    return reinterpret_cast<const void*>(&bwd_scalar_kernel<DT, OFF>);
 }
 template <bool OFF>
 static const void* bwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
     switch (p.dtype) {
-    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF32, OFF>(p.per_thread);
-    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF16, OFF>(p.per_thread);
-    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kBF16, OFF>(p.per_thread);
+    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF32, OFF>();
+    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF16, OFF>();
+    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kBF16, OFF>();
     default: return nullptr;
     }
 }

@@ -19,7 +19,9 @@
 //    same order. Output vectors go straight from registers to HBM with 16-byte
 //    coalesced stores.
 //  * fwd_scalar_kernel: any N and any element alignment; one CTA per row,
-//    element-strided scalar loads that stay coalesced across a warp.
+//    element-strided scalar loads that stay coalesced across a warp, two passes
+//    over the row (the second one is served by L1/L2), few registers so that
+//    many rows are in flight per SM.
 #include "device.cuh"
 #include "launch.h"
 
@@ -175,8 +177,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     }
 }
 
-template <int DT, int EPT, bool OFFSET>
-__global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const RowArgs a) {
+template <int DT, bool OFFSET>
+__global__ void __launch_bounds__(kScalarThreads) fwd_scalar_kernel(const RowArgs a) {
     using E = Elem<DT>;
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
@@ -187,35 +189,40 @@ __global__ void __launch_bounds__(kScalarMaxThreads) fwd_scalar_kernel(const Row
     const int N = a.N;
     griddep_wait();
 
-    float gv[EPT];
-#pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-        const int col = tid + k * nt;
-        float w = col < N ? E::ld(a.gamma, col) : 0.f;
-        gv[k] = OFFSET ? 1.0f + w : w;
-    }
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t base = row * static_cast<int64_t>(N);
-        float xv[EPT];
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int col = tid + k * nt;
-            xv[k] = col < N ? E::ld(a.x, base + col) : 0.f;
-            ss = fmaf(xv[k], xv[k], ss);
+        // pass 1: sum of squares, four independent loads in flight per thread
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int col = tid;
+        for (; col + 3 * nt < N; col += 4 * nt) {
+            const float v0 = E::ld(a.x, base + col);
+            const float v1 = E::ld(a.x, base + col + nt);
+            const float v2 = E::ld(a.x, base + col + 2 * nt);
+            const float v3 = E::ld(a.x, base + col + 3 * nt);
+            s0 = fmaf(v0, v0, s0);
+            s1 = fmaf(v1, v1, s1);
+            s2 = fmaf(v2, v2, s2);
+            s3 = fmaf(v3, v3, s3);
         }
-        ss = warp_allsum(ss);
-        if (lane == 0) red[parity][warp] = ss;
+        for (; col < N; col += nt) {
+            const float v = E::ld(a.x, base + col);
+            s0 = fmaf(v, v, s0);
+        }
+        const float ws = warp_allsum((s0 + s1) + (s2 + s3));
+        if (lane == 0) red[parity][warp] = ws;
         __syncthreads();
         float t = lane < nwarps ? red[parity][lane] : 0.f;
         t = warp_allsum(t);
         const float r = 1.0f / sqrtf(t / static_cast<float>(N) + a.eps);
         if (tid == 0) a.rstd_out[row] = r;
-#pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int col = tid + k * nt;
-            if (col < N) E::st(a.y, base + col, OFFSET ? (gv[k] * xv[k]) * r : (xv[k] * r) * gv[k]);
+        // pass 2: the row again (now in L1/L2), gamma, output
+#pragma unroll 4
+        for (int c = tid; c < N; c += nt) {
+            const float xv = E::ld(a.x, base + c);
+            const float w = E::ld(a.gamma, c);
+            const float g = OFFSET ? 1.0f + w : w;
+            E::st(a.y, base + c, OFFSET ? (g * xv) * r : (xv * r) * g);
         }
     }
     griddep_launch_dependents();
@@ -239,24 +246,16 @@ static const void* fwd_tma_for(int vpt, int cluster) {
     return cluster > 1 ? fwd_tma_vpt<DT, OFF, true>(vpt) : fwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
-static const void* fwd_scalar_for(int ept) {
-    switch (ept) {
-    case 1: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 1, OFF>);
-    case 2: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 2, OFF>);
-    case 4: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 4, OFF>);
-    case 8: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 8, OFF>);
-    case 16: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 16, OFF>);
-    case 32: return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, 32, OFF>);
-    default: return nullptr;
-    }
+static const void* fwd_scalar_for() {
+    return reinterpret_cast<const void*>(&fwd_scalar_kernel<DT, OFF>);
 }
 template <bool OFF>
 static const void* fwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
     switch (p.dtype) {
-    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF32, OFF>(p.per_thread);
-    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF16, OFF>(p.per_thread);
-    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kBF16, OFF>(p.per_thread);
+    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF32, OFF>();
+    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF16, OFF>();
+    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kBF16, OFF>();
     default: return nullptr;
     }
 }

@@ -28,11 +28,10 @@ struct RowArgs {
 enum PathKind : int { kPathTma = 0, kPathScalar = 1 };
 
 // Thread caps (also the kernels' __launch_bounds__): a TMA-path slice is at most
-// 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path holds up
-// to 32 elements per thread, so 512 threads cover N = 16384.
+// 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over
+// the row with 256 threads.
 constexpr int kTmaMaxThreads = 256;
-constexpr int kScalarMaxThreads = 512;
-constexpr int kScalarMaxPerThread = 32;
+constexpr int kScalarThreads = 256;
 
 // A launch shape chosen by the planner.
 struct Plan {
@@ -56,5 +55,8 @@ cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s);
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
                                  cudaStream_t s);
+
+// Device address of the error word on the current device (nullptr on failure).
+uint32_t* device_error_word();
 
 }  // namespace rmsnorm
