@@ -31,7 +31,9 @@
  *     inputs.
  *   - Pointers must be aligned to their element size. Rows whose byte length is
  *     a multiple of 16 with 16-byte-aligned x/y/dy/dx/gamma take the TMA bulk-copy
- *     path; anything else takes a general path with scalar loads. Both give
+ *     path; other rows of up to ~20 KB take a path with 16-byte loads of each
+ *     row's aligned span (when x and dy share their offset from a 16-byte
+ *     boundary); anything else takes a general path with scalar loads. All give
  *     results within the same correctness gate.
  *   - All calls are asynchronous on `stream` (NULL = legacy default stream).
  *     Validation happens on the host before any launch; when a call returns an
@@ -163,8 +165,10 @@ rmsnorm_status rmsnorm_selftest_wait_timeout(uint32_t polls, rmsnorm_stream_t st
 
 /*
  * Launch plan the library would use, as text (for logs and tests), e.g.
- * "tma cluster=1 threads=256 vpt=2 stages=6 blocks=456". pass: 0 = forward,
- * 1 = backward. aligned16: whether the data pointers will be 16-byte aligned.
+ * "tma cluster=1 threads=256 vpt=2 stages=2 units=456 ...". pass: 0 = forward,
+ * 1 = backward. aligned16: 1 if the data pointers will be 16-byte aligned, 0 if
+ * not (x and dy sharing their offset from a 16-byte boundary), 2 if x and dy
+ * sit at different offsets.
  * Writes at most buf_len bytes including the terminating NUL. Host-only.
  */
 rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,

@@ -154,9 +154,10 @@ def rmsnorm_selftest_wait_timeout(polls, stream=None) -> int:
 
 
 def rmsnorm_describe_plan(pass_, M, N, dtype, aligned16=True) -> str:
+    """aligned16: True/1 aligned, False/0 shared 16-byte offset, 2 mixed offsets."""
     buf = ctypes.create_string_buffer(256)
     st = _load().rmsnorm_describe_plan(int(pass_), int(M), int(N), _dtype_code(dtype),
-                                       int(bool(aligned16)), buf, 256)
+                                       int(aligned16), buf, 256)
     if st != RMSNORM_OK:
         raise RMSNormError(st, "rmsnorm_describe_plan")
     return buf.value.decode()

@@ -201,19 +201,66 @@ bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     return true;
 }
 
+// Row-vector path: rows that are not 16-byte multiples or start off a 16-byte
+// boundary, up to kRowVecMaxKv vectors per thread; as many blocks as fit.
+bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    const int64_t rowb = static_cast<int64_t>(N) * elem_bytes(dt);
+    const int64_t nvr = rowb / 16 + 2;
+    const int need = static_cast<int>(ceil_div(nvr, kScalarThreads));
+    int kv = 0;
+    for (int cand : {1, 2, 3, 5})
+        if (cand >= need) {
+            kv = cand;
+            break;
+        }
+    if (kv == 0 || kv > kRowVecMaxKv) return false;
+    p.path = kPathRowVec;
+    p.dtype = dt;
+    p.offset = offset;
+    p.cluster = 1;
+    p.threads = kScalarThreads;
+    p.per_thread = kv;
+    p.stages = 0;
+    // gamma (and the backward's accumulators) with one padding word per 8 columns
+    const size_t padded = static_cast<size_t>(N) + N / 8 + 1;
+    p.smem = padded * 4 * (pass == 0 ? 1 : 2);
+    const void* k = rowvec_kernel(pass, p);
+    if (!k || !prepare_kernel(k, dev, di)) return false;
+    int64_t units = 0;
+    if (!occupancy_units(k, p, di, 0, units)) return false;
+    if (pass == 1) {
+        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
+        if (units > cap) units = cap;
+    }
+    p.units = units < M ? units : M;
+    return true;
+}
+
+// layout: kLayoutAligned (x, y/dy/dx and gamma 16-byte aligned), kLayoutPhase
+// (x and, for the backward, dy share a 16-byte phase), kLayoutMixed (anything else).
+enum Layout : int { kLayoutMixed = 0, kLayoutAligned = 1, kLayoutPhase = 2 };
+
 // Caller holds g_mu.
-bool get_plan(int pass, int64_t M, int N, int dt, int offset, bool aligned16, int dev, const DeviceInfo& di,
+bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int dev, const DeviceInfo& di,
               Plan& p) {
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
-    const int path = (aligned16 && tma_shape) ? kPathTma : kPathScalar;
-    auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, 0, g_override_gen);
+    int path = kPathScalar;
+    if (layout == kLayoutAligned && tma_shape) path = kPathTma;
+    else if (layout != kLayoutMixed) path = kPathRowVec;
+    auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         p = it->second;
         return true;
     }
-    const bool ok = path == kPathTma ? plan_tma(pass, M, N, dt, offset, dev, di, p)
-                                     : plan_scalar(pass, M, N, dt, offset, dev, di, p);
+    bool ok = false;
+    if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
+    else if (path == kPathRowVec) ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);
+    if (!ok && path == kPathRowVec) {
+        (void)cudaGetLastError();
+        path = kPathScalar;  // rows too wide for the row-vector kernels
+    }
+    if (path == kPathScalar) ok = plan_scalar(pass, M, N, dt, offset, dev, di, p);
     if (!ok) {
         (void)cudaGetLastError();  // leave no stale runtime error behind
         return false;
@@ -265,13 +312,14 @@ extern "C" rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y,
     if (!x || !gamma || !y || !rstd) return RMSNORM_ERR_NULL;
     const size_t s = elem_bytes(dtype);
     if (!aligned(x, s) || !aligned(gamma, s) || !aligned(y, s) || !aligned(rstd, 4)) return RMSNORM_ERR_ALIGN;
-    const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16);
+    // the forward's row-vector path reads x by its own phase and writes y at any phase
+    const int layout = (aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16)) ? kLayoutAligned : kLayoutPhase;
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
     DeviceInfo* di = nullptr;
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(0, M, static_cast<int>(N), dtype, offset, a16, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    if (!get_plan(0, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
     RowArgs a = {};
     a.x = x;
     a.gamma = gamma;
@@ -294,9 +342,9 @@ extern "C" size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype
     if (current_device(dev, di) != RMSNORM_OK) return 0;
     int64_t units = 0;
     Plan p;
-    for (int a16 = 0; a16 < 2; ++a16)
+    for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
         for (int off = 0; off < 2; ++off)
-            if (get_plan(1, M, static_cast<int>(N), dtype, off, a16 != 0, dev, *di, p) && p.units > units)
+            if (get_plan(1, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
                 units = p.units;
     return static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
 }
@@ -324,10 +372,14 @@ extern "C" rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void*
     if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(rstd, 4) ||
         !aligned(workspace, 16))
         return RMSNORM_ERR_ALIGN;
-    const bool a16 = aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16);
+    // the backward's row-vector path reads x and dy with one mapping: same 16-byte phase
+    const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15);
+    const int layout = (aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16))
+                           ? kLayoutAligned
+                           : (same_phase ? kLayoutPhase : kLayoutMixed);
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, a16, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
     const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -384,9 +436,13 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
     DeviceInfo* di = nullptr;
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(pass, M > 0 ? M : 1, static_cast<int>(N), dtype, 0, aligned16 != 0, dev, *di, p))
+    const int layout = aligned16 == 1 ? kLayoutAligned : (aligned16 == 0 ? kLayoutPhase : kLayoutMixed);
+    if (!get_plan(pass, M > 0 ? M : 1, static_cast<int>(N), dtype, 0, layout, dev, *di, p))
         return RMSNORM_ERR_UNSUPPORTED;
-    if (p.path == kPathTma)
+    if (p.path == kPathRowVec)
+        snprintf(buf, buf_len, "rowvec threads=%d kv=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
+                 static_cast<long long>(p.units), p.smem, di->sms);
+    else if (p.path == kPathTma)
         snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.cluster,
                  p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
     else

@@ -361,7 +361,10 @@ static const void* bwd_pick(const Plan& p) {
     }
 }
 
-const void* bwd_kernel(const Plan& p) { return p.offset ? bwd_pick<true>(p) : bwd_pick<false>(p); }
+const void* bwd_kernel(const Plan& p) {
+    if (p.path == kPathRowVec) return rowvec_kernel(1, p);
+    return p.offset ? bwd_pick<true>(p) : bwd_pick<false>(p);
+}
 
 const void* dgamma_reduce_kernel_ptr(int dtype) {
     switch (dtype) {

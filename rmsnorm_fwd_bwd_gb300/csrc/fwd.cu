@@ -260,7 +260,10 @@ static const void* fwd_pick(const Plan& p) {
     }
 }
 
-const void* fwd_kernel(const Plan& p) { return p.offset ? fwd_pick<true>(p) : fwd_pick<false>(p); }
+const void* fwd_kernel(const Plan& p) {
+    if (p.path == kPathRowVec) return rowvec_kernel(0, p);
+    return p.offset ? fwd_pick<true>(p) : fwd_pick<false>(p);
+}
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
     const void* k = fwd_kernel(p);

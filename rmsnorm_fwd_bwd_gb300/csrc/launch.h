@@ -25,7 +25,10 @@ struct RowArgs {
     uint32_t* err;         // device error word
 };
 
-enum PathKind : int { kPathTma = 0, kPathScalar = 1 };
+enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2 };
+
+// Most 16-byte vectors per thread on the row-vector path (256 threads).
+constexpr int kRowVecMaxKv = 5;
 
 // Thread caps (also the kernels' __launch_bounds__): a TMA-path slice is at most
 // 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over
@@ -49,6 +52,7 @@ struct Plan {
 // Kernel entry for a plan (used for occupancy queries and attributes).
 const void* fwd_kernel(const Plan& p);
 const void* bwd_kernel(const Plan& p);
+const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backward
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);

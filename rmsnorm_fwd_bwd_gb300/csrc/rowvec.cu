@@ -1,0 +1,342 @@
+// rowvec.cu -- forward and backward for rows that do not start on a 16-byte
+// boundary (N * sizeof(dtype) not a multiple of 16, e.g. bf16 N = 4099), with
+// the same formulas as fwd.cu / bwd.cu.
+//
+// A row starting at byte B covers the 16-byte aligned vectors from
+// floor16(B) to ceil16(B + N*s). Thread t loads vectors t, t + nt, ... of that
+// range with 16-byte loads; element e of vector v is column
+// c = (16 v - (B mod 16)) / s + e, and elements with c outside [0, N) belong to
+// the neighbouring rows and are masked to zero. A vector that would reach
+// before the tensor's first byte or past its last byte is loaded element by
+// element, so every access stays inside the tensor. The next row of the block
+// is loaded into registers while the current one is reduced (one row of
+// prefetch). Gamma (or 1 + w) is staged once per block in shared memory as fp32
+// indexed by column. Outputs with the same 16-byte phase as x get 16-byte
+// stores for vectors that lie wholly inside the row and element stores at the
+// row's two ends (never touching a neighbour's elements); outputs with another
+// phase are written element by element.
+#include "device.cuh"
+#include "launch.h"
+
+namespace rmsnorm {
+
+namespace {
+
+template <int DT> struct Raw;
+template <> struct Raw<kF32> {
+    __device__ __forceinline__ static uint32_t ld(const char* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+};
+template <> struct Raw<kF16> {
+    __device__ __forceinline__ static uint32_t ld(const char* p) {
+        return __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+};
+template <> struct Raw<kBF16> {
+    __device__ __forceinline__ static uint32_t ld(const char* p) {
+        return __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+};
+
+// The 16-byte vector at address A (16-byte aligned) with every element outside
+// the row [rb, re) set to zero. [tb, te) is the whole tensor: a vector that
+// reaches outside it is read element by element, so no byte outside the tensor
+// is touched.
+template <int DT>
+__device__ __forceinline__ uint4 load_vec(const char* A, const char* rb, const char* re, const char* tb,
+                                          const char* te) {
+    using E = Elem<DT>;
+    if (A >= rb && A + 16 <= re) return __ldg(reinterpret_cast<const uint4*>(A));  // wholly inside the row
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (A >= tb && A + 16 <= te) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(A));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e) {
+            const char* p = A + e * E::kBytes;
+            if (p < rb || p >= re) {
+                if (E::kBytes == 4) w[e] = 0u;
+                else w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
+            }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) {
+        const char* p = A + e * E::kBytes;
+        if (p >= rb && p < re) {
+            const uint32_t v = Raw<DT>::ld(p);
+            if (E::kBytes == 4) w[e] = v;
+            else w[e >> 1] |= v << ((e & 1) * 16);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Load the vectors of one row that thread tid owns (tid, tid + nt, ...); the
+// row spans (ceil16(re) - floor16(rb)) / 16 vectors, the rest are zero.
+template <int DT, int KV>
+__device__ __forceinline__ void load_row(const char* base, int64_t row, size_t rowb, int nt, int tid,
+                                         const char* tb, const char* te, uint4 (&v)[KV]) {
+    const char* rb = base + static_cast<size_t>(row) * rowb;
+    const char* re = rb + rowb;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(rb) & ~uintptr_t(15);
+    const int nv = static_cast<int>(((reinterpret_cast<uintptr_t>(re) + 15) & ~uintptr_t(15)) - a0) / 16;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        v[k] = idx < nv ? load_vec<DT>(reinterpret_cast<const char*>(a0) + 16 * idx, rb, re, tb, te)
+                        : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Shared-memory slot of column c. A thread owns 8 (or 4) consecutive columns, so
+// for one element position the 32 lanes of a warp touch columns 8 apart; one
+// padding word after every 8 columns puts those 32 accesses in 32 different
+// banks whatever the row's phase.
+__device__ __forceinline__ int pad_col(int c) { return c + (c >> 3); }
+
+}  // namespace
+
+template <int DT, int KV, bool OFFSET>
+__global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    constexpr int S = E::kBytes;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* gsm = reinterpret_cast<float*>(smem);  // gamma by pad_col(column)
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const int N = a.N;
+    const size_t rowb = static_cast<size_t>(N) * S;
+    const char* xb = static_cast<const char*>(a.x);
+    const char* xe = xb + static_cast<size_t>(a.M) * rowb;
+    char* yb = static_cast<char*>(a.y);
+    griddep_wait();
+
+    for (int c = tid; c < N; c += nt) {
+        const float w = E::ld(a.gamma, c);
+        gsm[pad_col(c)] = OFFSET ? 1.0f + w : w;
+    }
+    __syncthreads();
+
+    // vectors spanned by any row: at most rowb/16 + 2 (bounds the store loop)
+    const int nvr = static_cast<int>(rowb / 16) + 2;
+    uint4 cur[KV], nxt[KV];
+    int64_t row = blockIdx.x;
+    if (row < a.M) load_row<DT, KV>(xb, row, rowb, nt, tid, xb, xe, cur);
+    int parity = 0;
+    for (; row < a.M; row += gridDim.x, parity ^= 1) {
+        const int64_t next = row + gridDim.x;
+        if (next < a.M) load_row<DT, KV>(xb, next, rowb, nt, tid, xb, xe, nxt);
+        const char* rb = xb + static_cast<size_t>(row) * rowb;
+        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // row's byte phase
+        // column of element 0 of vector idx: (16*idx - o) / S
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            float f[VEC];
+            E::unpack(cur[k], f);
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                ss0 = fmaf(f[e], f[e], ss0);  // elements outside the row were loaded as zero
+                ss1 = fmaf(f[e + 1], f[e + 1], ss1);
+            }
+        }
+        const float wsum = warp_allsum(ss0 + ss1);
+        if (lane == 0) red[parity][warp] = wsum;
+        __syncthreads();
+        float t = lane < nwarps ? red[parity][lane] : 0.f;
+        t = warp_allsum(t);
+        const float r = 1.0f / sqrtf(t / static_cast<float>(N) + a.eps);
+        if (tid == 0) a.rstd_out[row] = r;
+
+        char* yrow = yb + static_cast<size_t>(row) * rowb;
+        const bool same_phase = (reinterpret_cast<uintptr_t>(yrow) & 15) == static_cast<uintptr_t>(o);
+        char* ya0 = reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(yrow) & ~uintptr_t(15));
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + k * nt;
+            if (idx >= nvr) continue;
+            const int c0 = (16 * idx - o) / S;
+            float f[VEC], out[VEC];
+            E::unpack(cur[k], f);
+            bool full = true;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int c = c0 + e;
+                const bool in = c >= 0 && c < N;
+                full = full && in;
+                const float g = in ? gsm[pad_col(c)] : 0.f;
+                out[e] = OFFSET ? (g * f[e]) * r : (f[e] * r) * g;
+            }
+            if (full && same_phase) {
+                stg128(ya0 + 16 * idx, E::pack(out));
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int c = c0 + e;
+                    if (c >= 0 && c < N) E::st(yrow, c, out[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KV; ++k) cur[k] = nxt[k];
+    }
+    griddep_launch_dependents();
+}
+
+template <int DT, int KV, bool OFFSET>
+__global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    constexpr int S = E::kBytes;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int padded = pad_col(a.N) + 1;
+    float* gsm = reinterpret_cast<float*>(smem);  // gamma (or 1 + w) by pad_col(column)
+    float* acc = gsm + padded;                    // dgamma accumulators by pad_col(column)
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const int N = a.N;
+    const size_t rowb = static_cast<size_t>(N) * S;
+    const char* xb = static_cast<const char*>(a.x);
+    const char* xe = xb + static_cast<size_t>(a.M) * rowb;
+    const char* db = static_cast<const char*>(a.dy);
+    const char* de = db + static_cast<size_t>(a.M) * rowb;
+    char* dxb = static_cast<char*>(a.dx);
+    griddep_wait();
+
+    for (int c = tid; c < N; c += nt) {
+        const float w = E::ld(a.gamma, c);
+        gsm[pad_col(c)] = OFFSET ? 1.0f + w : w;
+        acc[pad_col(c)] = 0.f;
+    }
+    __syncthreads();
+
+    const int nvr = static_cast<int>(rowb / 16) + 2;
+    uint4 cx[KV], cd[KV], nx[KV], nd[KV];
+    int64_t row = blockIdx.x;
+    if (row < a.M) {
+        load_row<DT, KV>(xb, row, rowb, nt, tid, xb, xe, cx);
+        load_row<DT, KV>(db, row, rowb, nt, tid, db, de, cd);
+    }
+    float r_next = row < a.M ? __ldg(a.rstd_in + row) : 0.f;
+    int parity = 0;
+    for (; row < a.M; row += gridDim.x, parity ^= 1) {
+        const int64_t next = row + gridDim.x;
+        const float r = r_next;
+        if (next < a.M) {
+            load_row<DT, KV>(xb, next, rowb, nt, tid, xb, xe, nx);
+            load_row<DT, KV>(db, next, rowb, nt, tid, db, de, nd);
+            r_next = __ldg(a.rstd_in + next);
+        }
+        const char* rb = xb + static_cast<size_t>(row) * rowb;
+        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + k * nt;
+            if (idx >= nvr) continue;
+            const int c0 = (16 * idx - o) / S;
+            float xf[VEC], df[VEC];
+            E::unpack(cx[k], xf);
+            E::unpack(cd[k], df);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int c = c0 + e;
+                if (c >= 0 && c < N) {
+                    const int sc = pad_col(c);
+                    const float u = __fmul_rn(df[e], gsm[sc]);
+                    if (e & 1) p1 = fmaf(u, xf[e], p1); else p0 = fmaf(u, xf[e], p0);
+                    acc[sc] = fmaf(__fmul_rn(df[e], xf[e]), r, acc[sc]);
+                }
+            }
+        }
+        const float wsum = warp_allsum(p0 + p1);
+        if (lane == 0) red[parity][warp] = wsum;
+        __syncthreads();
+        float t = lane < nwarps ? red[parity][lane] : 0.f;
+        t = warp_allsum(t);
+        const float cmean = t / static_cast<float>(N);
+        const float kk = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), cmean);  // dx = r*u - x*kk
+
+        char* dxrow = dxb + static_cast<size_t>(row) * rowb;
+        const bool same_phase = (reinterpret_cast<uintptr_t>(dxrow) & 15) == static_cast<uintptr_t>(o);
+        char* da0 = reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(dxrow) & ~uintptr_t(15));
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + k * nt;
+            if (idx >= nvr) continue;
+            const int c0 = (16 * idx - o) / S;
+            float xf[VEC], df[VEC], out[VEC];
+            E::unpack(cx[k], xf);
+            E::unpack(cd[k], df);
+            bool full = true;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const int c = c0 + e;
+                const bool in = c >= 0 && c < N;
+                full = full && in;
+                const float u = __fmul_rn(df[e], in ? gsm[pad_col(c)] : 0.f);
+                out[e] = fmaf(-xf[e], kk, __fmul_rn(r, u));
+            }
+            if (full && same_phase) {
+                stg128(da0 + 16 * idx, E::pack(out));
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const int c = c0 + e;
+                    if (c >= 0 && c < N) E::st(dxrow, c, out[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            cx[k] = nx[k];
+            cd[k] = nd[k];
+        }
+    }
+    griddep_launch_dependents();
+    __syncthreads();  // the last row's accumulator updates are done
+    if (blockIdx.x < a.M) {
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        for (int c = tid; c < N; c += nt) wrow[c] = acc[pad_col(c)];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+template <int DT, bool OFF>
+static const void* rowvec_pick(int pass, int kv) {
+#define RMSNORM_RV(K)                                                                          \
+    case K:                                                                                    \
+        return pass == 0 ? reinterpret_cast<const void*>(&fwd_rowvec_kernel<DT, K, OFF>)       \
+                         : reinterpret_cast<const void*>(&bwd_rowvec_kernel<DT, K, OFF>);
+    switch (kv) {
+        RMSNORM_RV(1)
+        RMSNORM_RV(2)
+        RMSNORM_RV(3)
+        RMSNORM_RV(5)
+    default: return nullptr;
+    }
+#undef RMSNORM_RV
+}
+
+const void* rowvec_kernel(int pass, const Plan& p) {
+    switch (p.dtype) {
+    case kF32: return p.offset ? rowvec_pick<kF32, true>(pass, p.per_thread) : rowvec_pick<kF32, false>(pass, p.per_thread);
+    case kF16: return p.offset ? rowvec_pick<kF16, true>(pass, p.per_thread) : rowvec_pick<kF16, false>(pass, p.per_thread);
+    case kBF16: return p.offset ? rowvec_pick<kBF16, true>(pass, p.per_thread) : rowvec_pick<kBF16, false>(pass, p.per_thread);
+    default: return nullptr;
+    }
+}
+
+}  // namespace rmsnorm

@@ -50,16 +50,20 @@ def _place(arr, dtype, misalign):
 
 def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, stream=None):
     """Forward (and backward) through the C ABI. Returns numpy storage arrays
-    (y, rstd, dx, dgamma); dx/dgamma are None when do_bwd is False."""
+    (y, rstd, dx, dgamma); dx/dgamma are None when do_bwd is False.
+
+    misalign: False, True (every tensor one element off a 16-byte boundary) or a
+    set of names among {"x", "g", "dy", "y", "dx"} to shift only those."""
     torch = _torch()
     M, N = x.shape
+    names = {"x", "g", "dy", "y", "dx"} if misalign is True else set(misalign or ())
     keep = []
-    _, xt = _place(x, dtype, misalign); keep.append(_)
-    _, gt = _place(g, dtype, misalign); keep.append(_)
-    _, dyt = _place(dy, dtype, misalign); keep.append(_)
+    _, xt = _place(x, dtype, "x" in names); keep.append(_)
+    _, gt = _place(g, dtype, "g" in names); keep.append(_)
+    _, dyt = _place(dy, dtype, "dy" in names); keep.append(_)
     ybuf, y = _guarded(M * N, dtype)
     rbuf, rstd = _guarded(M, "float32")
-    if misalign:
+    if "y" in names:
         ybuf2 = torch.empty(M * N + 2 * GUARD + 1, dtype=y.dtype, device=y.device)
         ybuf2[1:] = ybuf
         ybuf, y = ybuf2[1:], ybuf2[1 + GUARD:1 + GUARD + M * N]
@@ -70,7 +74,7 @@ def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, st
     if do_bwd:
         dxbuf, dxt = _guarded(M * N, dtype)
         dgbuf, dgt = _guarded(N, dtype)
-        if misalign:
+        if "dx" in names:
             b2 = torch.empty(M * N + 2 * GUARD + 1, dtype=dxt.dtype, device=dxt.device)
             b2[1:] = dxbuf
             dxbuf, dxt = b2[1:], b2[1 + GUARD:1 + GUARD + M * N]

@@ -118,6 +118,15 @@ def test_misaligned_pointers_take_general_path(dtype, N, offset):
     _gate_case(x, g, dy, dtype, offset=offset, misalign=True)
 
 
+@pytest.mark.parametrize("names", [("y",), ("dx",), ("y", "dx"), ("dy",), ("x",), ("g",)])
+@pytest.mark.parametrize("dtype,N", [("bfloat16", 4096), ("bfloat16", 4099), ("float32", 1023)])
+def test_partially_misaligned_tensors(names, dtype, N):
+    """Outputs at another 16-byte phase than x (element stores at every vector),
+    and x/dy at different phases (general scalar path)."""
+    x, g, dy = inputs.make_inputs(37, N, dtype, seed=len(names) + N)
+    _gate_case(x, g, dy, dtype, misalign=set(names), title=f"{dtype} N={N} shifted={names}")
+
+
 def test_many_rows_narrow():
     for M, N, dtype in ((100003, 64, "float32"), (50001, 8, "bfloat16"), (20011, 24, "float16")):
         x, g, dy = inputs.make_inputs(M, N, dtype, seed=3)
@@ -230,8 +239,11 @@ def test_plan_dispatch():
     assert B.rmsnorm_describe_plan(1, 65536, 4096, "bfloat16").startswith("tma cluster=1")
     assert B.rmsnorm_describe_plan(0, 16384, 16384, "float32").startswith("tma cluster=4")
     assert B.rmsnorm_describe_plan(1, 16384, 16384, "float16").startswith("tma cluster=2")
-    assert B.rmsnorm_describe_plan(0, 8192, 4099, "bfloat16").startswith("scalar")
-    assert B.rmsnorm_describe_plan(0, 8192, 4096, "bfloat16", aligned16=False).startswith("scalar")
+    assert B.rmsnorm_describe_plan(0, 8192, 4099, "bfloat16").startswith("rowvec")
+    assert B.rmsnorm_describe_plan(1, 8192, 4099, "bfloat16").startswith("rowvec")
+    assert B.rmsnorm_describe_plan(0, 8192, 4096, "bfloat16", aligned16=False).startswith("rowvec")
+    assert B.rmsnorm_describe_plan(1, 8192, 4096, "bfloat16", aligned16=2).startswith("scalar")
+    assert B.rmsnorm_describe_plan(0, 64, 16383, "float32", aligned16=False).startswith("scalar")
 
 
 def test_torch_conveniences_match_raw_calls():
