@@ -1,0 +1,112 @@
+"""PyTorch integration of the C-ABI kernels: autograd and torch.library ops.
+
+``rms_norm(x, weight, eps, offset)`` runs the library's forward kernel and, in
+the backward pass, its fused backward kernels -- the same calls as
+``binding.rmsnorm_fwd`` / ``binding.rmsnorm_bwd``, with tensors allocated by
+torch. It is registered as the custom ops ``rmsnorm_gb300::fwd`` and
+``rmsnorm_gb300::bwd`` (with fake-tensor shapes and an autograd formula), so it
+traces without graph breaks.
+
+Mirrors the autograd adapter of the page "Check an AI model calculation before
+accelerating it" (section "Connecting Autograd and actually training"): the
+forward saves x, gamma and the per-row r; the backward returns dx and dgamma and
+nothing for eps; ``CALLS`` counts passes through the adapter so a training loop
+can prove it ran the kernel path.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding
+
+CALLS = {"forward": 0, "backward": 0}
+
+
+def _rows(x: torch.Tensor):
+    N = x.shape[-1]
+    return (x.numel() // N if N else 0), N
+
+
+@torch.library.custom_op("rmsnorm_gb300::fwd", mutates_args=())
+def _fwd(x: torch.Tensor, weight: torch.Tensor, eps: float, offset: bool) -> tuple[torch.Tensor, torch.Tensor]:
+    x = x.contiguous()
+    M, N = _rows(x)
+    y = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = binding.rmsnorm_fwd(x, weight, y, rstd, M, N, eps, x.dtype, int(offset),
+                             torch.cuda.current_stream(x.device))
+    if st != binding.RMSNORM_OK:
+        raise binding.RMSNormError(st, "rmsnorm_fwd")
+    CALLS["forward"] += 1
+    return y, rstd
+
+
+@_fwd.register_fake
+def _(x, weight, eps, offset):
+    return torch.empty_like(x), x.new_empty(x.shape[:-1], dtype=torch.float32)
+
+
+@torch.library.custom_op("rmsnorm_gb300::bwd", mutates_args=())
+def _bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, rstd: torch.Tensor,
+         offset: bool) -> tuple[torch.Tensor, torch.Tensor]:
+    dy = dy.contiguous()
+    x = x.contiguous()
+    M, N = _rows(x)
+    need = binding.rmsnorm_bwd_workspace_size(M, N, x.dtype)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(weight)
+    st = binding.rmsnorm_bwd(dy, x, weight, rstd, dx, dw, M, N, x.dtype, int(offset), ws, ws.numel(),
+                             torch.cuda.current_stream(x.device))
+    if st != binding.RMSNORM_OK:
+        raise binding.RMSNormError(st, "rmsnorm_bwd")
+    CALLS["backward"] += 1
+    return dx, dw
+
+
+@_bwd.register_fake
+def _(dy, x, weight, rstd, offset):
+    return torch.empty_like(x), torch.empty_like(weight)
+
+
+def _setup_context(ctx, inputs, output):
+    x, weight, eps, offset = inputs
+    _, rstd = output
+    ctx.save_for_backward(x, weight, rstd)
+    ctx.offset = offset
+
+
+def _backward(ctx, dy, drstd):
+    del drstd  # rstd is an auxiliary output; no gradient flows through it
+    x, weight, rstd = ctx.saved_tensors
+    dx, dw = _bwd(dy, x, weight, rstd, ctx.offset)
+    return dx, dw, None, None
+
+
+_fwd.register_autograd(_backward, setup_context=_setup_context)
+
+
+def rms_norm(x: torch.Tensor, weight: torch.Tensor, eps: float = 1e-6, offset: bool = False) -> torch.Tensor:
+    """y = x * r * weight (offset: x * r * (1 + weight)), r = 1/sqrt(mean(x^2, -1) + eps)."""
+    if x.shape[-1] != weight.shape[-1] or weight.dim() != 1:
+        raise ValueError("weight must be 1-D with x.shape[-1] elements")
+    if x.dtype != weight.dtype:
+        raise ValueError("x and weight must share a dtype")
+    y, _ = torch.ops.rmsnorm_gb300.fwd(x, weight, float(eps), bool(offset))
+    return y
+
+
+class RMSNorm(torch.nn.Module):
+    """Drop-in module: a learned weight of ``normalized_shape`` elements (ones,
+    or zeros for the offset variant, so that both start as the identity scale)."""
+
+    def __init__(self, normalized_shape: int, eps: float = 1e-6, offset: bool = False,
+                 device=None, dtype=None):
+        super().__init__()
+        self.eps = eps
+        self.offset = offset
+        init = torch.zeros if offset else torch.ones
+        self.weight = torch.nn.Parameter(init(normalized_shape, device=device, dtype=dtype))
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return rms_norm(x, self.weight, self.eps, self.offset)
