@@ -26,17 +26,22 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per tensor
-// Default ring: 2 stages, at most 3 resident blocks per SM. Measured on GB300
-// (bf16, N = 4096): deeper rings and more blocks put more requests in flight
-// and lower HBM throughput; 2 x 3 reaches the TMA-copy ceiling.
-constexpr int kDefaultStages = 2;
-constexpr int kDefaultBlocksPerSm = 3;
-constexpr int kDefaultThreadCap[2] = {256, 128};  // forward, backward
-// Rows split over a cluster pay a cluster barrier per row; measured on GB300
-// (fp16/fp32, N = 8192-16384) a third stage and more resident blocks hide it.
+// Default TMA plans, from timing grids on GB300 over row sizes 4-64 KB:
+//  - every thread owns at least 2 vectors of a row (the per-row reductions,
+//    barrier and square root are then amortised over >= 16 bf16 elements);
+//  - the ring bytes resident per SM (stages x stage bytes x blocks) sit near
+//    kRingPerSm: more requests in flight lower HBM efficiency, fewer leave it
+//    latency-bound. The forward keeps 2 stages; the backward 2-4.
+constexpr int kMinVpt = 2;
+constexpr int kThreadCap[2] = {256, 128};  // forward, backward (no cluster)
+constexpr int kMaxElemsPerThread = 32;     // backward: keeps x, u and dgamma sums in registers
+constexpr int kRingPerSm[2] = {48 << 10, 96 << 10};
+constexpr int kMaxBlocksPerSm = 16;
+// Rows split over a cluster pay a cluster barrier per row; there a third
+// forward stage and more resident blocks hide it better (measured).
+constexpr int kClusterThreadCap[2] = {128, 256};
 constexpr int kClusterStages[2] = {3, 2};
 constexpr int kClusterBlocksPerSm[2] = {6, 3};
-constexpr int kClusterThreadCap[2] = {128, 256};
 // Bound on the general path's backward workspace; more blocks than this add
 // little once every SM holds one.
 constexpr int64_t kScalarWorkspaceCap = int64_t(8) << 20;
@@ -141,22 +146,42 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kDefaultThreadCap[pass]);
-        for (vpt = 1; vpt <= 8; vpt *= 2)
+        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kThreadCap[pass]);
+        for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
+        if (pass == 1 && cl == 1)
+            while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread &&
+                   round_up(ceil_div(nvec, vpt / 2), 32) <= kTmaMaxThreads)
+                vpt /= 2;  // more threads rather than more registers
+        while (vpt > 1 && ceil_div(nvec, vpt / 2) <= 32) vpt /= 2;  // tiny rows: one warp
     }
     if (vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8) return false;
     int threads = ov.threads ? ov.threads : static_cast<int>(round_up(ceil_div(nvec, vpt), 32));
     if (threads < 32) threads = 32;
     if (threads % 32 != 0 || threads > kTmaMaxThreads) return false;
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
-    if ((threads / 32) * cl > 32) return false;
+    if (cl > 8) return false;
     const int slice = (N / cl) * s;
     const int stage = (pass == 0 ? 1 : 2) * slice;
-    // warp partials, abort flag (+ the backward's fp32 gamma slice)
+    // mbarriers, warp partials, abort flag (+ the backward's fp32 gamma slice)
     const int fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : (N / cl) * 4);
-    int stages = ov.stages ? ov.stages : (cl > 1 ? kClusterStages[pass] : kDefaultStages);
+    // ring shape: blocks per SM and stages aiming at kRingPerSm resident per SM
+    int bps = ov.blocks_per_sm;
+    int stages = ov.stages;
+    if (cl > 1) {
+        if (!stages) stages = kClusterStages[pass];
+        if (!bps) bps = kClusterBlocksPerSm[pass];
+    } else if (pass == 0) {
+        if (!stages) stages = 2;
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[0], 2 * stage), 2),
+                                                           kMaxBlocksPerSm));
+    } else {
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (2 * stage), 1), 4));
+        if (!stages)
+            stages = static_cast<int>(
+                std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (static_cast<int64_t>(bps) * stage), 2), 4));
+    }
     while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
     if (stages < 1) return false;
     p.path = kPathTma;
@@ -170,7 +195,6 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
-    const int bps = ov.blocks_per_sm ? ov.blocks_per_sm : (cl > 1 ? kClusterBlocksPerSm[pass] : kDefaultBlocksPerSm);
     if (!occupancy_units(k, p, di, bps, units)) return false;
     p.units = units < M ? units : M;
     return true;
