@@ -143,6 +143,28 @@ rmsnorm_status rmsnorm_bwd_static_scratch(const void* dy, const void* x, const v
                                           int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
                                           rmsnorm_stream_t stream);
 
+/*
+ * Strided forms: the same operations on row-major tensors whose consecutive
+ * rows are ld* elements apart (ld* >= N; the gaps between rows are neither read
+ * nor written), e.g. a view of the first N columns of a wider matrix. With
+ * ld* = N they are rmsnorm_fwd / rmsnorm_bwd. The fast paths need every row to
+ * start on the same 16-byte boundary pattern: 16-byte aligned rows take the TMA
+ * path; x and dy rows at equal offsets from a 16-byte boundary the row-vector
+ * path; other combinations the general path. The workspace of
+ * rmsnorm_bwd_strided is sized by rmsnorm_bwd_workspace_size(M, N, dtype).
+ * Extension of the pages' contract, which rejects non-contiguous inputs
+ * ("Check an AI model calculation before accelerating it", section "Adapting
+ * the kernel and moving to production", which names strides as the first
+ * extension to build and test).
+ */
+rmsnorm_status rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
+                                   float* rstd, int64_t M, int64_t N, float eps, rmsnorm_dtype dtype,
+                                   int offset, rmsnorm_stream_t stream);
+rmsnorm_status rmsnorm_bwd_strided(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                                   const void* gamma, const float* rstd, void* dx, int64_t lddx,
+                                   void* dgamma, int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
+                                   void* workspace, size_t workspace_bytes, rmsnorm_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 const char* rmsnorm_status_string(rmsnorm_status status);
 

@@ -65,6 +65,8 @@ def _load():
             "rmsnorm_set_launch_override": (I, [I, I, I, I, I]),
             "rmsnorm_bwd_static_scratch": (I, [P, P, P, P, P, P, I64, I64, I, I, P]),
             "rmsnorm_selftest_wait_timeout": (I, [ctypes.c_uint32, P]),
+            "rmsnorm_fwd_strided": (I, [P, I64, P, P, I64, P, I64, I64, F, I, I, P]),
+            "rmsnorm_bwd_strided": (I, [P, I64, P, I64, P, P, P, I64, P, I64, I64, I, I, P, SZ, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -115,6 +117,20 @@ def _stream(s):
 def rmsnorm_fwd(x, gamma, y, rstd, M, N, eps, dtype, offset, stream=None) -> int:
     return _load().rmsnorm_fwd(_addr(x), _addr(gamma), _addr(y), _addr(rstd), int(M), int(N),
                                float(eps), _dtype_code(dtype), int(offset), _stream(stream))
+
+
+def rmsnorm_fwd_strided(x, ldx, gamma, y, ldy, rstd, M, N, eps, dtype, offset, stream=None) -> int:
+    return _load().rmsnorm_fwd_strided(_addr(x), int(ldx), _addr(gamma), _addr(y), int(ldy), _addr(rstd),
+                                       int(M), int(N), float(eps), _dtype_code(dtype), int(offset),
+                                       _stream(stream))
+
+
+def rmsnorm_bwd_strided(dy, lddy, x, ldx, gamma, rstd, dx, lddx, dgamma, M, N, dtype, offset, workspace,
+                        workspace_bytes, stream=None) -> int:
+    return _load().rmsnorm_bwd_strided(_addr(dy), int(lddy), _addr(x), int(ldx), _addr(gamma), _addr(rstd),
+                                       _addr(dx), int(lddx), _addr(dgamma), int(M), int(N),
+                                       _dtype_code(dtype), int(offset), _addr(workspace),
+                                       int(workspace_bytes), _stream(stream))
 
 
 def rmsnorm_bwd_workspace_size(M, N, dtype) -> int:

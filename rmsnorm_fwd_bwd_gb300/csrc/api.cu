@@ -326,18 +326,30 @@ uint32_t* device_error_word() {
 
 using namespace rmsnorm;
 
-extern "C" rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
-                                      int64_t N, float eps, rmsnorm_dtype dtype, int offset,
-                                      rmsnorm_stream_t stream) {
+namespace rmsnorm {
+namespace {
+
+bool pitch_ok(int64_t ld, int64_t N, int64_t M, size_t s) {
+    // ld >= N, and the whole span (M - 1) * ld + N elements addressable
+    return ld >= N && ld <= (int64_t(1) << 40) / static_cast<int64_t>(s) &&
+           (M <= 1 || (M - 1) <= (int64_t(1) << 46) / ld);
+}
+
+rmsnorm_status fwd_impl(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy, float* rstd, int64_t M,
+                        int64_t N, float eps, rmsnorm_dtype dtype, int offset, rmsnorm_stream_t stream) {
     rmsnorm_status st = check_common(M, N, dtype, offset);
     if (st != RMSNORM_OK) return st;
     if (!std::isfinite(eps) || !(eps > 0.0f)) return RMSNORM_ERR_EPS;
+    const size_t s = elem_bytes(dtype);
+    if (!pitch_ok(ldx, N, M, s) || !pitch_ok(ldy, N, M, s)) return RMSNORM_ERR_SHAPE;
     if (M == 0) return RMSNORM_OK;
     if (!x || !gamma || !y || !rstd) return RMSNORM_ERR_NULL;
-    const size_t s = elem_bytes(dtype);
     if (!aligned(x, s) || !aligned(gamma, s) || !aligned(y, s) || !aligned(rstd, 4)) return RMSNORM_ERR_ALIGN;
-    // the forward's row-vector path reads x by its own phase and writes y at any phase
-    const int layout = (aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16)) ? kLayoutAligned : kLayoutPhase;
+    // TMA path: 16-byte aligned rows; otherwise the forward's row-vector path,
+    // which reads x at each row's own phase and writes y at any phase
+    const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16) && (ldx * s) % 16 == 0 &&
+                     (ldy * s) % 16 == 0;
+    const int layout = a16 ? kLayoutAligned : kLayoutPhase;
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
     DeviceInfo* di = nullptr;
@@ -351,11 +363,84 @@ extern "C" rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y,
     a.rstd_out = rstd;
     a.M = M;
     a.N = static_cast<int>(N);
+    a.ldx = ldx;
+    a.ldy = ldy;
     a.eps = eps;
     a.stages = p.stages;
     a.err = di->err;
     if (launch_fwd(p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
+}
+
+rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx, const void* gamma,
+                        const float* rstd, void* dx, int64_t lddx, void* dgamma, int64_t M, int64_t N,
+                        rmsnorm_dtype dtype, int offset, void* workspace, size_t workspace_bytes,
+                        rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, offset);
+    if (st != RMSNORM_OK) return st;
+    const size_t s = elem_bytes(dtype);
+    if (!pitch_ok(ldx, N, M, s) || !pitch_ok(lddy, N, M, s) || !pitch_ok(lddx, N, M, s)) return RMSNORM_ERR_SHAPE;
+    if (!dgamma) return RMSNORM_ERR_NULL;
+    if (!aligned(dgamma, s)) return RMSNORM_ERR_ALIGN;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (M == 0) {
+        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
+    if (!dy || !x || !gamma || !rstd || !dx || !workspace) return RMSNORM_ERR_NULL;
+    if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(rstd, 4) ||
+        !aligned(workspace, 16))
+        return RMSNORM_ERR_ALIGN;
+    // TMA path: 16-byte aligned rows; row-vector path: x and dy rows at the same
+    // 16-byte phase (same pointer phase and pitches equal modulo 16 bytes);
+    // anything else: the general path
+    const bool a16 = aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16) &&
+                     (ldx * s) % 16 == 0 && (lddy * s) % 16 == 0 && (lddx * s) % 16 == 0;
+    const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15) &&
+                            (ldx * s) % 16 == (lddy * s) % 16;
+    const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.dy = dy;
+    a.rstd_in = rstd;
+    a.dx = dx;
+    a.ws = static_cast<float*>(workspace);
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.ldx = ldx;
+    a.lddy = lddy;
+    a.lddx = lddx;
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_bwd(p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+}  // namespace rmsnorm
+
+extern "C" rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
+                                      int64_t N, float eps, rmsnorm_dtype dtype, int offset,
+                                      rmsnorm_stream_t stream) {
+    return fwd_impl(x, N, gamma, y, N, rstd, M, N, eps, dtype, offset, stream);
+}
+
+extern "C" rmsnorm_status rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* gamma, void* y, int64_t ldy,
+                                              float* rstd, int64_t M, int64_t N, float eps, rmsnorm_dtype dtype,
+                                              int offset, rmsnorm_stream_t stream) {
+    return fwd_impl(x, ldx, gamma, y, ldy, rstd, M, N, eps, dtype, offset, stream);
 }
 
 extern "C" size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype) {
@@ -377,49 +462,16 @@ extern "C" rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void*
                                       void* dx, void* dgamma, int64_t M, int64_t N, rmsnorm_dtype dtype,
                                       int offset, void* workspace, size_t workspace_bytes,
                                       rmsnorm_stream_t stream) {
-    rmsnorm_status st = check_common(M, N, dtype, offset);
-    if (st != RMSNORM_OK) return st;
-    if (!dgamma) return RMSNORM_ERR_NULL;
-    const size_t s = elem_bytes(dtype);
-    if (!aligned(dgamma, s)) return RMSNORM_ERR_ALIGN;
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
-    if (M == 0) {
-        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs) != cudaSuccess)
-            return RMSNORM_ERR_CUDA;
-        return RMSNORM_OK;
-    }
-    if (!dy || !x || !gamma || !rstd || !dx || !workspace) return RMSNORM_ERR_NULL;
-    if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(rstd, 4) ||
-        !aligned(workspace, 16))
-        return RMSNORM_ERR_ALIGN;
-    // the backward's row-vector path reads x and dy with one mapping: same 16-byte phase
-    const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15);
-    const int layout = (aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16))
-                           ? kLayoutAligned
-                           : (same_phase ? kLayoutPhase : kLayoutMixed);
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
-    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
-    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
-    RowArgs a = {};
-    a.x = x;
-    a.gamma = gamma;
-    a.dy = dy;
-    a.rstd_in = rstd;
-    a.dx = dx;
-    a.ws = static_cast<float*>(workspace);
-    a.M = M;
-    a.N = static_cast<int>(N);
-    a.stages = p.stages;
-    a.err = di->err;
-    if (launch_bwd(p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    return RMSNORM_OK;
+    return bwd_impl(dy, N, x, N, gamma, rstd, dx, N, dgamma, M, N, dtype, offset, workspace, workspace_bytes,
+                    stream);
+}
+
+extern "C" rmsnorm_status rmsnorm_bwd_strided(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                                              const void* gamma, const float* rstd, void* dx, int64_t lddx,
+                                              void* dgamma, int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
+                                              void* workspace, size_t workspace_bytes, rmsnorm_stream_t stream) {
+    return bwd_impl(dy, lddy, x, ldx, gamma, rstd, dx, lddx, dgamma, M, N, dtype, offset, workspace,
+                    workspace_bytes, stream);
 }
 
 extern "C" const char* rmsnorm_status_string(rmsnorm_status status) {

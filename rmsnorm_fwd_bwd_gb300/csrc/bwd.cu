@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
     const int nvec = ns / VEC;
     const uint32_t slice_bytes = static_cast<uint32_t>(ns) * E::kBytes;
     const uint32_t stage_bytes = 2 * slice_bytes;  // x slice, then dy slice
-    const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
+    const size_t x_pitch = static_cast<size_t>(a.ldx) * E::kBytes;
+    const size_t dy_pitch = static_cast<size_t>(a.lddy) * E::kBytes;
+    const size_t dx_pitch = static_cast<size_t>(a.lddx) * E::kBytes;
     const int S = a.stages;
 
     // shared memory: ring | gamma slice in fp32 | mbarriers | warp partials [2][32] | abort flag
@@ -91,10 +93,10 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
 
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
-        const size_t off = static_cast<size_t>(cid + j * ncl) * row_bytes;
+        const size_t r = static_cast<size_t>(cid + j * ncl);
         mbar_arrive_expect_tx(bar, stage_bytes);
-        bulk_g2s(smem_u32(st), xsl + off, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + slice_bytes), dysl + off, slice_bytes, bar, pol);
+        bulk_g2s(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol);
+        bulk_g2s(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a
         const float k = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), c);
 
         if (!aborted) {
-            char* dxrow = dxsl + static_cast<size_t>(row) * row_bytes;
+            char* dxrow = dxsl + static_cast<size_t>(row) * dx_pitch;
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const int idx = v * nt + tid;
@@ -236,14 +238,16 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
     for (int c = tid; c < N; c += nt) acc[c] = 0.f;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
-        const int64_t base = row * static_cast<int64_t>(N);
+        const int64_t base = row * a.ldx;
+        const int64_t dbase = row * a.lddy;
+        const int64_t obase = row * a.lddx;
         const float r = __ldg(a.rstd_in + row);
         // pass 1: sum of u*x, and this row's dgamma terms
         float p0 = 0.f, p1 = 0.f;
         int col = tid;
         for (; col + nt < N; col += 2 * nt) {
             const float x0 = E::ld(a.x, base + col), x1 = E::ld(a.x, base + col + nt);
-            const float d0 = E::ld(a.dy, base + col), d1 = E::ld(a.dy, base + col + nt);
+            const float d0 = E::ld(a.dy, dbase + col), d1 = E::ld(a.dy, dbase + col + nt);
             const float w0 = E::ld(a.gamma, col), w1 = E::ld(a.gamma, col + nt);
             p0 = fmaf(__fmul_rn(d0, OFFSET ? 1.0f + w0 : w0), x0, p0);
             p1 = fmaf(__fmul_rn(d1, OFFSET ? 1.0f + w1 : w1), x1, p1);
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
         }
         for (; col < N; col += nt) {
             const float x0 = E::ld(a.x, base + col);
-            const float d0 = E::ld(a.dy, base + col);
+            const float d0 = E::ld(a.dy, dbase + col);
             const float w0 = E::ld(a.gamma, col);
             p0 = fmaf(__fmul_rn(d0, OFFSET ? 1.0f + w0 : w0), x0, p0);
             acc[col] = fmaf(__fmul_rn(d0, x0), r, acc[col]);
@@ -268,10 +272,10 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 #pragma unroll 4
         for (int cc = tid; cc < N; cc += nt) {
             const float xv = E::ld(a.x, base + cc);
-            const float dv = E::ld(a.dy, base + cc);
+            const float dv = E::ld(a.dy, dbase + cc);
             const float w = E::ld(a.gamma, cc);
             const float u = __fmul_rn(dv, OFFSET ? 1.0f + w : w);
-            E::st(a.dx, base + cc, fmaf(-xv, k, __fmul_rn(r, u)));
+            E::st(a.dx, obase + cc, fmaf(-xv, k, __fmul_rn(r, u)));
         }
     }
     griddep_launch_dependents();

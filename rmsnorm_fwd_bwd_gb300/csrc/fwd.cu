@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     const int ns = a.N / static_cast<int>(csize);  // slice width (elements)
     const int nvec = ns / VEC;                       // 16-byte vectors per slice
     const uint32_t slice_bytes = static_cast<uint32_t>(ns) * E::kBytes;
-    const size_t row_bytes = static_cast<size_t>(a.N) * E::kBytes;
+    const size_t x_pitch = static_cast<size_t>(a.ldx) * E::kBytes;
+    const size_t y_pitch = static_cast<size_t>(a.ldy) * E::kBytes;
     const int S = a.stages;
 
     // shared memory: ring | mbarriers | warp partials [2][32] | abort flag
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
         for (int64_t j = 0; j < pre; ++j) {
             const uint32_t bar = smem_u32(&full[j]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * row_bytes,
+            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
                      slice_bytes, bar, pol);
         }
     }
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
             fence_proxy_async_smem();
             const uint32_t bar = smem_u32(&full[s]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * row_bytes, slice_bytes, bar, pol);
+            bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * x_pitch, slice_bytes, bar, pol);
         }
         if (++s == S) {
             s = 0;
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
 
         if (!aborted) {
             if (tid == 0 && crank == 0) a.rstd_out[row] = r;
-            char* yrow = ysl + static_cast<size_t>(row) * row_bytes;
+            char* yrow = ysl + static_cast<size_t>(row) * y_pitch;
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const int idx = v * nt + tid;
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_scalar_kernel(const RowArg
 
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
-        const int64_t base = row * static_cast<int64_t>(N);
+        const int64_t base = row * a.ldx;
+        const int64_t ybase = row * a.ldy;
         // pass 1: sum of squares, four independent loads in flight per thread
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
         int col = tid;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_scalar_kernel(const RowArg
             const float xv = E::ld(a.x, base + c);
             const float w = E::ld(a.gamma, c);
             const float g = OFFSET ? 1.0f + w : w;
-            E::st(a.y, base + c, OFFSET ? (g * xv) * r : (xv * r) * g);
+            E::st(a.y, ybase + c, OFFSET ? (g * xv) * r : (xv * r) * g);
         }
     }
     griddep_launch_dependents();

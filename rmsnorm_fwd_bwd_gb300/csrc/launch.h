@@ -20,6 +20,7 @@ struct RowArgs {
     float* ws;             // backward: dgamma partials [units][N]
     int64_t M;
     int N;
+    int64_t ldx, ldy, lddy, lddx;  // row pitches in elements (>= N)
     float eps;
     int stages;            // TMA pipeline depth
     uint32_t* err;         // device error word

@@ -3,7 +3,8 @@
 // the same formulas as fwd.cu / bwd.cu.
 //
 // A row starting at byte B covers the 16-byte aligned vectors from
-// floor16(B) to ceil16(B + N*s). Thread t loads vectors t, t + nt, ... of that
+// floor16(B) to ceil16(B + N*s) (rows may be further apart than N elements:
+// each tensor has its own row pitch). Thread t loads vectors t, t + nt, ... of that
 // range with 16-byte loads; element e of vector v is column
 // c = (16 v - (B mod 16)) / s + e, and elements with c outside [0, N) belong to
 // the neighbouring rows and are masked to zero. A vector that would reach
@@ -75,9 +76,9 @@ __device__ __forceinline__ uint4 load_vec(const char* A, const char* rb, const c
 // Load the vectors of one row that thread tid owns (tid, tid + nt, ...); the
 // row spans (ceil16(re) - floor16(rb)) / 16 vectors, the rest are zero.
 template <int DT, int KV>
-__device__ __forceinline__ void load_row(const char* base, int64_t row, size_t rowb, int nt, int tid,
-                                         const char* tb, const char* te, uint4 (&v)[KV]) {
-    const char* rb = base + static_cast<size_t>(row) * rowb;
+__device__ __forceinline__ void load_row(const char* base, int64_t row, size_t pitch, size_t rowb, int nt,
+                                         int tid, const char* tb, const char* te, uint4 (&v)[KV]) {
+    const char* rb = base + static_cast<size_t>(row) * pitch;
     const char* re = rb + rowb;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(rb) & ~uintptr_t(15);
     const int nv = static_cast<int>(((reinterpret_cast<uintptr_t>(re) + 15) & ~uintptr_t(15)) - a0) / 16;
@@ -112,8 +113,10 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     const int nwarps = nt >> 5;
     const int N = a.N;
     const size_t rowb = static_cast<size_t>(N) * S;
+    const size_t xp = static_cast<size_t>(a.ldx) * S;
+    const size_t yp = static_cast<size_t>(a.ldy) * S;
     const char* xb = static_cast<const char*>(a.x);
-    const char* xe = xb + static_cast<size_t>(a.M) * rowb;
+    const char* xe = xb + static_cast<size_t>(a.M - 1) * xp + rowb;  // last byte of the tensor + 1
     char* yb = static_cast<char*>(a.y);
     griddep_wait();
 
@@ -127,12 +130,12 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     const int nvr = static_cast<int>(rowb / 16) + 2;
     uint4 cur[KV], nxt[KV];
     int64_t row = blockIdx.x;
-    if (row < a.M) load_row<DT, KV>(xb, row, rowb, nt, tid, xb, xe, cur);
+    if (row < a.M) load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cur);
     int parity = 0;
     for (; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t next = row + gridDim.x;
-        if (next < a.M) load_row<DT, KV>(xb, next, rowb, nt, tid, xb, xe, nxt);
-        const char* rb = xb + static_cast<size_t>(row) * rowb;
+        if (next < a.M) load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nxt);
+        const char* rb = xb + static_cast<size_t>(row) * xp;
         const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // row's byte phase
         // column of element 0 of vector idx: (16*idx - o) / S
         float ss0 = 0.f, ss1 = 0.f;
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
         const float r = 1.0f / sqrtf(t / static_cast<float>(N) + a.eps);
         if (tid == 0) a.rstd_out[row] = r;
 
-        char* yrow = yb + static_cast<size_t>(row) * rowb;
+        char* yrow = yb + static_cast<size_t>(row) * yp;
         const bool same_phase = (reinterpret_cast<uintptr_t>(yrow) & 15) == static_cast<uintptr_t>(o);
         char* ya0 = reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(yrow) & ~uintptr_t(15));
 #pragma unroll
@@ -206,10 +209,13 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     const int nwarps = nt >> 5;
     const int N = a.N;
     const size_t rowb = static_cast<size_t>(N) * S;
+    const size_t xp = static_cast<size_t>(a.ldx) * S;
+    const size_t dp = static_cast<size_t>(a.lddy) * S;
+    const size_t op = static_cast<size_t>(a.lddx) * S;
     const char* xb = static_cast<const char*>(a.x);
-    const char* xe = xb + static_cast<size_t>(a.M) * rowb;
+    const char* xe = xb + static_cast<size_t>(a.M - 1) * xp + rowb;
     const char* db = static_cast<const char*>(a.dy);
-    const char* de = db + static_cast<size_t>(a.M) * rowb;
+    const char* de = db + static_cast<size_t>(a.M - 1) * dp + rowb;
     char* dxb = static_cast<char*>(a.dx);
     griddep_wait();
 
@@ -224,8 +230,8 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     uint4 cx[KV], cd[KV], nx[KV], nd[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) {
-        load_row<DT, KV>(xb, row, rowb, nt, tid, xb, xe, cx);
-        load_row<DT, KV>(db, row, rowb, nt, tid, db, de, cd);
+        load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cx);
+        load_row<DT, KV>(db, row, dp, rowb, nt, tid, db, de, cd);
     }
     float r_next = row < a.M ? __ldg(a.rstd_in + row) : 0.f;
     int parity = 0;
@@ -233,12 +239,12 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
         const int64_t next = row + gridDim.x;
         const float r = r_next;
         if (next < a.M) {
-            load_row<DT, KV>(xb, next, rowb, nt, tid, xb, xe, nx);
-            load_row<DT, KV>(db, next, rowb, nt, tid, db, de, nd);
+            load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nx);
+            load_row<DT, KV>(db, next, dp, rowb, nt, tid, db, de, nd);
             r_next = __ldg(a.rstd_in + next);
         }
-        const char* rb = xb + static_cast<size_t>(row) * rowb;
-        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);
+        const char* rb = xb + static_cast<size_t>(row) * xp;
+        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // dy rows share it
         float p0 = 0.f, p1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
         const float cmean = t / static_cast<float>(N);
         const float kk = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), cmean);  // dx = r*u - x*kk
 
-        char* dxrow = dxb + static_cast<size_t>(row) * rowb;
+        char* dxrow = dxb + static_cast<size_t>(row) * op;
         const bool same_phase = (reinterpret_cast<uintptr_t>(dxrow) & 15) == static_cast<uintptr_t>(o);
         char* da0 = reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(dxrow) & ~uintptr_t(15));
 #pragma unroll
