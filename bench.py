@@ -12,7 +12,8 @@ value  = algorithmic bytes of all ranks' steps / max-over-ranks time, in GB/s,
          where fwd bytes = 2*M*N*s + N*s + 4*M and bwd bytes = 3*M*N*s + 2*N*s + 4*M.
 e2e    = the same metric through the C ABI with host buffers: each step copies
          x, gamma, dy from pinned host memory, runs both passes, and copies
-         y, rstd, dx, dgamma back.
+         y, rstd, dx, dgamma back (two streams take alternate steps so copies in
+         both directions overlap kernels).
 roofline = the backward pass (the dominant cost) against the measured HBM copy
          bandwidth in MEASURED_PEAKS.json.
 cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
@@ -323,38 +324,51 @@ def run_ours(args, w):
     step_bytes = w.fwd_bytes() + w.bwd_bytes()
     value = aggregate(step_bytes, K, world, secs)
 
-    # end to end through the C ABI with host buffers
-    y_h = torch.empty_like(x_h).pin_memory()
-    dx_h = torch.empty_like(x_h).pin_memory()
-    dg_h = torch.empty_like(g_h).pin_memory()
-    r_h = torch.empty(M, dtype=torch.float32).pin_memory()
-    xf, gf, dyf = x.view(-1), g, dy.view(-1)
+    # end to end through the C ABI with host buffers: every step copies its inputs
+    # in from pinned host memory and its results back out. Two streams with their
+    # own device buffers take alternate steps, so one step's copies overlap the
+    # other's kernels and copies in the opposite direction (NVLink-C2C is full
+    # duplex); the timed region covers all steps on both streams.
     e2e_steps = max(3, min(K, args.e2e_steps))
+    streams = [stream, torch.cuda.Stream(dev)]
+    sets = [dict(x=x, g=g, dy=dy, y=y, dx=dx, dg=dg, r=rstd, ws=ws)]
+    sets.append({k: torch.empty_like(v) for k, v in sets[0].items()})
+    houts = [dict(y=torch.empty_like(x_h).pin_memory(), dx=torch.empty_like(x_h).pin_memory(),
+                  dg=torch.empty_like(g_h).pin_memory(), r=torch.empty(M, dtype=torch.float32).pin_memory())
+             for _ in range(2)]
 
-    def e2e_step():
-        xf.copy_(x_h, non_blocking=True)
-        gf.copy_(g_h, non_blocking=True)
-        dyf.copy_(dy_h, non_blocking=True)
-        fwd()
-        bwd()
-        y_h.copy_(y.view(-1), non_blocking=True)
-        r_h.copy_(rstd, non_blocking=True)
-        dx_h.copy_(dx.view(-1), non_blocking=True)
-        dg_h.copy_(dg, non_blocking=True)
+    def e2e_step(k):
+        s, b, h = streams[k % 2], sets[k % 2], houts[k % 2]
+        with torch.cuda.stream(s):
+            b["x"].view(-1).copy_(x_h, non_blocking=True)
+            b["g"].copy_(g_h, non_blocking=True)
+            b["dy"].view(-1).copy_(dy_h, non_blocking=True)
+            st = B.rmsnorm_fwd(b["x"], b["g"], b["y"], b["r"], M, N, w.eps, dt, int(w.offset), s)
+            st = st or B.rmsnorm_bwd(b["dy"], b["x"], b["g"], b["r"], b["dx"], b["dg"], M, N, dt, int(w.offset),
+                                     b["ws"], wsz, s)
+            if st:
+                raise B.RMSNormError(st, "end-to-end step")
+            h["y"].copy_(b["y"].view(-1), non_blocking=True)
+            h["r"].copy_(b["r"], non_blocking=True)
+            h["dx"].copy_(b["dx"].view(-1), non_blocking=True)
+            h["dg"].copy_(b["dg"], non_blocking=True)
 
-    e2e_step()
+    e2e_step(0)
+    e2e_step(1)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize()
     e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
     h2d = (x_h.numel() + g_h.numel() + dy_h.numel()) * w.elem_bytes
-    d2h = (y_h.numel() + dx_h.numel() + dg_h.numel()) * w.elem_bytes + 4 * M
+    d2h = (x_h.numel() * 2 + g_h.numel()) * w.elem_bytes + 4 * M
 
     if rank != 0:
         return 0

@@ -1,11 +1,13 @@
 """PyTorch integration of the C-ABI kernels: autograd and torch.library ops.
 
 ``rms_norm(x, weight, eps, offset)`` runs the library's forward kernel and, in
-the backward pass, its fused backward kernels -- the same calls as
-``binding.rmsnorm_fwd`` / ``binding.rmsnorm_bwd``, with tensors allocated by
-torch. It is registered as the custom ops ``rmsnorm_gb300::fwd`` and
-``rmsnorm_gb300::bwd`` (with fake-tensor shapes and an autograd formula), so it
-traces without graph breaks.
+the backward pass, its fused backward kernels -- the calls
+``binding.rmsnorm_fwd_strided`` / ``binding.rmsnorm_bwd_strided``, with tensors
+allocated by torch. 2-D inputs whose rows are further apart than their length
+(e.g. ``big[:, :N]``) are passed with their row pitch, without a copy. It is
+registered as the custom ops ``rmsnorm_gb300::fwd`` and ``rmsnorm_gb300::bwd``
+(with fake-tensor shapes and an autograd formula), so it traces without graph
+breaks.
 
 Mirrors the autograd adapter of the page "Check an AI model calculation before
 accelerating it" (section "Connecting Autograd and actually training"): the
@@ -27,14 +29,23 @@ def _rows(x: torch.Tensor):
     return (x.numel() // N if N else 0), N
 
 
+def _row_view(t: torch.Tensor):
+    """(tensor, row pitch): 2-D views with unit column stride keep their row
+    pitch (no copy); anything else is made contiguous."""
+    if t.dim() == 2 and t.stride(1) == 1 and t.stride(0) >= t.shape[1] and t.shape[0] > 0:
+        return t, t.stride(0)
+    t = t.contiguous()
+    return t, t.shape[-1]
+
+
 @torch.library.custom_op("rmsnorm_gb300::fwd", mutates_args=())
 def _fwd(x: torch.Tensor, weight: torch.Tensor, eps: float, offset: bool) -> tuple[torch.Tensor, torch.Tensor]:
-    x = x.contiguous()
+    x, ldx = _row_view(x)
     M, N = _rows(x)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    st = binding.rmsnorm_fwd(x, weight, y, rstd, M, N, eps, x.dtype, int(offset),
-                             torch.cuda.current_stream(x.device))
+    st = binding.rmsnorm_fwd_strided(x, ldx, weight.contiguous(), y, N, rstd, M, N, eps, x.dtype,
+                                     int(offset), torch.cuda.current_stream(x.device))
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "rmsnorm_fwd")
     CALLS["forward"] += 1
@@ -43,21 +54,21 @@ def _fwd(x: torch.Tensor, weight: torch.Tensor, eps: float, offset: bool) -> tup
 
 @_fwd.register_fake
 def _(x, weight, eps, offset):
-    return torch.empty_like(x), x.new_empty(x.shape[:-1], dtype=torch.float32)
+    return x.new_empty(x.shape), x.new_empty(x.shape[:-1], dtype=torch.float32)
 
 
 @torch.library.custom_op("rmsnorm_gb300::bwd", mutates_args=())
 def _bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, rstd: torch.Tensor,
          offset: bool) -> tuple[torch.Tensor, torch.Tensor]:
-    dy = dy.contiguous()
-    x = x.contiguous()
+    dy, lddy = _row_view(dy)
+    x, ldx = _row_view(x)
     M, N = _rows(x)
     need = binding.rmsnorm_bwd_workspace_size(M, N, x.dtype)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    dx = torch.empty_like(x)
-    dw = torch.empty_like(weight)
-    st = binding.rmsnorm_bwd(dy, x, weight, rstd, dx, dw, M, N, x.dtype, int(offset), ws, ws.numel(),
-                             torch.cuda.current_stream(x.device))
+    dx = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    dw = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
+    st = binding.rmsnorm_bwd_strided(dy, lddy, x, ldx, weight.contiguous(), rstd.contiguous(), dx, N, dw, M, N,
+                                     x.dtype, int(offset), ws, ws.numel(), torch.cuda.current_stream(x.device))
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "rmsnorm_bwd")
     CALLS["backward"] += 1
@@ -66,7 +77,7 @@ def _bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, rstd: torch.Te
 
 @_bwd.register_fake
 def _(dy, x, weight, rstd, offset):
-    return torch.empty_like(x), torch.empty_like(weight)
+    return x.new_empty(x.shape), weight.new_empty(weight.shape)
 
 
 def _setup_context(ctx, inputs, output):

@@ -122,6 +122,28 @@ def test_opcheck_and_trace_without_graph_breaks(torch, ag):
     assert torch.equal(gx1, gx2) and torch.equal(gw1, gw2)
 
 
+def test_strided_view_passes_the_gate(torch, ag):
+    """A 2-D view of the first N columns of a wider tensor goes to the kernels
+    with its row pitch. (Its rows are not 16-byte multiples apart, so it takes
+    another kernel path than a contiguous copy would: the results agree within
+    the gate, not bit for bit.)"""
+    from rmsnorm_fwd_bwd_gb300 import binding as B
+    M, N, ld, dtype = 64, 1000, 1100, "bfloat16"
+    x, g, dy = inputs.make_inputs(M, N, dtype, seed=23)
+    big = torch.zeros(M, ld, device="cuda", dtype=torch.bfloat16)
+    big[:, :N] = B.to_device(x.reshape(-1), dtype).view(M, N)
+    xv = big[:, :N].detach().requires_grad_(True)
+    assert xv.stride() == (ld, 1)
+    w = B.to_device(g, dtype).requires_grad_(True)
+    y = ag.rms_norm(xv, w)
+    y.backward(B.to_device(dy.reshape(-1), dtype).view(M, N))
+    res = check.gate_outputs(x, g, dy, dtype, False, 1e-6,
+                             y=B.to_numpy(y, dtype).reshape(M, N),
+                             dx=B.to_numpy(xv.grad, dtype).reshape(M, N),
+                             dgamma=B.to_numpy(w.grad, dtype))
+    assert gate.overall(res) == "PASS", gate.report("autograd strided view", res)
+
+
 def test_module_rejects_mismatched_weight(torch, ag):
     x = torch.randn(4, 32, device="cuda")
     with pytest.raises(ValueError):
