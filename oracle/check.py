@@ -73,3 +73,52 @@ def gate_outputs(x, g, dy, dtype, offset, eps, y=None, rstd=None, dx=None, dgamm
         out.append(gate.check("dgamma", dgg, orc.decode(dgr, dtype), tgt, dtype, rel_bound=rel,
                               condition=cond))
     return out
+
+
+def gate_ln_outputs(x, g, b, dy, dtype, eps, y=None, mean=None, rstd=None, dx=None, dgamma=None,
+                    dbeta=None, rows=None):
+    """LayerNorm counterpart of ``gate_outputs``: gates whichever of y, mean,
+    rstd, dx (all rows, or ``rows`` only), dgamma and dbeta are given.
+    Returns a list of ``gate.GateResult``."""
+    out = []
+    xs = x if rows is None else np.ascontiguousarray(x[rows])
+    dys = dy if rows is None else np.ascontiguousarray(dy[rows])
+    rel = _rel_bound(dtype)
+    fp32 = gate.FP32_MAX_RELATIVE_ERROR
+    if y is not None or mean is not None or rstd is not None:
+        yg, mg, rg = orc.ln_fwd_golden(xs, g, b, dtype, eps=eps, want_y=y is not None)
+        yr, mr, rr = orc.ln_fwd_reference(xs, g, b, dtype, eps=eps)
+        if y is not None:
+            out.append(gate.check("y", yg, orc.decode(yr, dtype), orc.decode(y, dtype), dtype,
+                                  rel_bound=rel))
+        if mean is not None:
+            out.append(gate.check("mean", mg, mr.astype(np.float64), np.asarray(mean, np.float64),
+                                  "float32", rel_bound=fp32))
+        if rstd is not None:
+            out.append(gate.check("rstd", rg, rr.astype(np.float64), np.asarray(rstd, np.float64),
+                                  "float32", rel_bound=fp32))
+    if dx is not None:
+        dxg, _, _ = orc.ln_bwd_golden(dys, xs, g, dtype, eps=eps)
+        dxr, _, _ = orc.ln_bwd_reference(dys, xs, g, dtype, eps=eps)
+        out.append(gate.check("dx", dxg, orc.decode(dxr, dtype), orc.decode(dx, dtype), dtype,
+                              rel_bound=rel))
+    if dgamma is not None or dbeta is not None:
+        _, dgg, dbg = orc.ln_bwd_golden(dy, x, g, dtype, eps=eps, want_dx=False)
+        _, dgr, dbr = orc.ln_bwd_reference(dy, x, g, dtype, eps=eps, want_dx=False)
+        _, mg, rg = orc.ln_fwd_golden(x, g, b, dtype, eps=eps, want_y=False)
+        for name, gold, ref, tgt in (("dgamma", dgg, dgr, dgamma), ("dbeta", dbg, dbr, dbeta)):
+            if tgt is None:
+                continue
+            tgt = orc.decode(tgt, dtype)
+            cond = None
+            if x.shape[0]:
+                col = gate.worst_index(gold, tgt)
+                dyc = orc.decode(np.ascontiguousarray(dy[:, col]), dtype)
+                if name == "dgamma":
+                    xc = orc.decode(np.ascontiguousarray(x[:, col]), dtype)
+                    cond = gate.condition_number(dyc * (xc - mg) * rg)
+                else:
+                    cond = gate.condition_number(dyc)
+            out.append(gate.check(name, gold, orc.decode(ref, dtype), tgt, dtype, rel_bound=rel,
+                                  condition=cond))
+    return out

@@ -36,6 +36,12 @@ PARITY = {
     "bwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
     "round/encode/decode": "pinned: numpy float16 and torch bfloat16 conversions, "
                            "hand-picked ties and overflow",
+    "ln_fwd_golden": "pinned: hand-worked 4-element row, constant row, N=1, shift and "
+                     "scale invariance, zero-mean rows match the RMSNorm golden",
+    "ln_bwd_golden": "pinned: finite differences of the golden forward, per-row sums of dx "
+                     "vanish, dbeta = column sums of dy, hand-worked 2-element row",
+    "ln_fwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
+    "ln_bwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
 }
 
 _lock = threading.Lock()
@@ -75,6 +81,10 @@ def _load():
             "oracle_bwd_golden": [P, P, P, I64, I64, D, I, I, P, P],
             "oracle_fwd_reference": [P, P, I64, I64, F, I, I, P, P],
             "oracle_bwd_reference": [P, P, P, I64, I64, F, I, I, P, P],
+            "oracle_ln_fwd_golden": [P, P, P, I64, I64, D, I, P, P, P],
+            "oracle_ln_bwd_golden": [P, P, P, I64, I64, D, I, P, P, P],
+            "oracle_ln_fwd_reference": [P, P, P, I64, I64, F, I, P, P, P],
+            "oracle_ln_bwd_reference": [P, P, P, I64, I64, F, I, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -178,3 +188,62 @@ def bwd_reference(dy, x, gamma, dtype, eps=1e-6, offset=False, want_dx=True):
     _load().oracle_bwd_reference(_ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
                                  DTYPES[dtype], int(bool(offset)), _ptr(dx), _ptr(dg))
     return dx, dg
+
+
+# --------------------------------------------------------------------------- #
+# LayerNorm (golden fp64; reference in the I/O dtype with fp32 intermediates)
+# --------------------------------------------------------------------------- #
+def ln_fwd_golden(x, gamma, beta, dtype, eps=1e-5, want_y=True):
+    """Returns ``(y fp64 [M,N] or None, mean fp64 [M], rstd fp64 [M])``."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    gamma = _check(gamma, dtype, (N,))
+    beta = _check(beta, dtype, (N,))
+    y = np.empty((M, N), np.float64) if want_y else None
+    mean = np.empty(M, np.float64)
+    rstd = np.empty(M, np.float64)
+    _load().oracle_ln_fwd_golden(_ptr(x), _ptr(gamma), _ptr(beta), M, N, float(eps),
+                                 DTYPES[dtype], _ptr(y), _ptr(mean), _ptr(rstd))
+    return y, mean, rstd
+
+
+def ln_bwd_golden(dy, x, gamma, dtype, eps=1e-5, want_dx=True):
+    """Returns ``(dx fp64 [M,N] or None, dgamma fp64 [N], dbeta fp64 [N])``."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    dy = _check(dy, dtype, (M, N))
+    gamma = _check(gamma, dtype, (N,))
+    dx = np.empty((M, N), np.float64) if want_dx else None
+    dg = np.empty(N, np.float64)
+    db = np.empty(N, np.float64)
+    _load().oracle_ln_bwd_golden(_ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
+                                 DTYPES[dtype], _ptr(dx), _ptr(dg), _ptr(db))
+    return dx, dg, db
+
+
+def ln_fwd_reference(x, gamma, beta, dtype, eps=1e-5):
+    """Returns ``(y [M,N] in dtype storage, mean float32 [M], rstd float32 [M])``."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    gamma = _check(gamma, dtype, (N,))
+    beta = _check(beta, dtype, (N,))
+    y = np.empty((M, N), STORAGE[dtype])
+    mean = np.empty(M, np.float32)
+    rstd = np.empty(M, np.float32)
+    _load().oracle_ln_fwd_reference(_ptr(x), _ptr(gamma), _ptr(beta), M, N, float(eps),
+                                    DTYPES[dtype], _ptr(y), _ptr(mean), _ptr(rstd))
+    return y, mean, rstd
+
+
+def ln_bwd_reference(dy, x, gamma, dtype, eps=1e-5, want_dx=True):
+    """Returns ``(dx or None, dgamma, dbeta)`` in dtype storage."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    dy = _check(dy, dtype, (M, N))
+    gamma = _check(gamma, dtype, (N,))
+    dx = np.empty((M, N), STORAGE[dtype]) if want_dx else None
+    dg = np.empty(N, STORAGE[dtype])
+    db = np.empty(N, STORAGE[dtype])
+    _load().oracle_ln_bwd_reference(_ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
+                                    DTYPES[dtype], _ptr(dx), _ptr(dg), _ptr(db))
+    return dx, dg, db

@@ -335,3 +335,159 @@ void oracle_bwd_reference(const void* dy, const void* x, const void* gamma, int6
         free(acc);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* LayerNorm (page "torch.compile performance leap: optimizing LayerNorm and  */
+/* RMSNorm kernels", sections 1.1 "LayerNorm" and 2 "Backward": per-row mean  */
+/* and variance, learned gamma and beta; gradients for the input, the weight  */
+/* and the bias). The pages print no formula; this is the standard one:       */
+/*     mu = mean_j x_j;  var = mean_j (x_j - mu)^2;  r = 1/sqrt(var + eps)     */
+/*     xhat = (x - mu) * r;  y = xhat * gamma + beta                          */
+/*     u = dy * gamma;  dx = r * (u - mean_j u_j - xhat * mean_j(u_j xhat_j))  */
+/*     dgamma = sum_rows dy * xhat;  dbeta = sum_rows dy                       */
+/* The variance is the two-pass one (mean first).                             */
+/* ------------------------------------------------------------------------- */
+
+/* y[M*N], mean[M], rstd[M] in fp64 (any of them may be NULL). */
+void oracle_ln_fwd_golden(const void* x, const void* gamma, const void* beta, int64_t M, int64_t N,
+                          double eps, int dt, double* y, double* mean, double* rstd) {
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += load_elem(x, row + j, dt);
+        const double mu = s / (double)N;
+        double v = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double d = load_elem(x, row + j, dt) - mu;
+            v += d * d;
+        }
+        const double r = 1.0 / sqrt(v / (double)N + eps);
+        if (mean) mean[i] = mu;
+        if (rstd) rstd[i] = r;
+        if (!y) continue;
+        for (int64_t j = 0; j < N; ++j) {
+            const double xh = (load_elem(x, row + j, dt) - mu) * r;
+            y[row + j] = xh * load_elem(gamma, j, dt) + load_elem(beta, j, dt);
+        }
+    }
+}
+
+/* dx[M*N] (may be NULL), dgamma[N], dbeta[N] in fp64; mu and r recomputed from x. */
+void oracle_ln_bwd_golden(const void* dy, const void* x, const void* gamma, int64_t M, int64_t N, double eps,
+                          int dt, double* dx, double* dgamma, double* dbeta) {
+    for (int64_t j = 0; j < N; ++j) {
+        if (dgamma) dgamma[j] = 0.0;
+        if (dbeta) dbeta[j] = 0.0;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        double mu, r;
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += load_elem(x, row + j, dt);
+        mu = s / (double)N;
+        double v = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double d = load_elem(x, row + j, dt) - mu;
+            v += d * d;
+        }
+        r = 1.0 / sqrt(v / (double)N + eps);
+        double su = 0.0, suxh = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double u = load_elem(dy, row + j, dt) * load_elem(gamma, j, dt);
+            const double xh = (load_elem(x, row + j, dt) - mu) * r;
+            su += u;
+            suxh += u * xh;
+        }
+        const double mean_u = su / (double)N, mean_uxh = suxh / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            const double dyv = load_elem(dy, row + j, dt);
+            const double u = dyv * load_elem(gamma, j, dt);
+            const double xh = (load_elem(x, row + j, dt) - mu) * r;
+            if (dx) dx[row + j] = r * (u - mean_u - xh * mean_uxh);
+            if (dgamma) dgamma[j] += dyv * xh;
+            if (dbeta) dbeta[j] += dyv;
+        }
+    }
+}
+
+/* fp32 mean and r of one row: sequential sums, two-pass variance. */
+static void ln_row_stats_f32(const void* x, int64_t row, int64_t N, float eps, int dt, float* mu_out,
+                             float* r_out) {
+    float s = 0.0f;
+    for (int64_t j = 0; j < N; ++j) s = s + ld32(x, row + j, dt);
+    const float mu = s / (float)N;
+    float v = 0.0f;
+    for (int64_t j = 0; j < N; ++j) {
+        const float d = ld32(x, row + j, dt) - mu;
+        const float d2 = d * d;
+        v = v + d2;
+    }
+    const float var = v / (float)N;
+    const float den = sqrtf(var + eps);
+    *mu_out = mu;
+    *r_out = 1.0f / den;
+}
+
+/* y[M*N] in dtype dt, mean[M] and rstd[M] fp32. y = ((x - mu) * r) * gamma + beta. */
+void oracle_ln_fwd_reference(const void* x, const void* gamma, const void* beta, int64_t M, int64_t N,
+                             float eps, int dt, void* y, float* mean, float* rstd) {
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        float mu, r;
+        ln_row_stats_f32(x, row, N, eps, dt, &mu, &r);
+        if (mean) mean[i] = mu;
+        if (rstd) rstd[i] = r;
+        if (!y) continue;
+        for (int64_t j = 0; j < N; ++j) {
+            const float d = ld32(x, row + j, dt) - mu;
+            const float xh = d * r;
+            const float t = xh * ld32(gamma, j, dt);
+            const float out = t + ld32(beta, j, dt);
+            store_elem(y, row + j, dt, (double)out);
+        }
+    }
+}
+
+/* dx[M*N] (may be NULL), dgamma[N], dbeta[N] in dtype dt; fp32 intermediates,
+ * sequential sums; dx = r * ((u - mean(u)) - xhat * mean(u*xhat)). */
+void oracle_ln_bwd_reference(const void* dy, const void* x, const void* gamma, int64_t M, int64_t N, float eps,
+                             int dt, void* dx, void* dgamma, void* dbeta) {
+    float* ag = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    float* ab = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    for (int64_t j = 0; j < N; ++j) ag[j] = ab[j] = 0.0f;
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        float mu, r;
+        ln_row_stats_f32(x, row, N, eps, dt, &mu, &r);
+        float su = 0.0f, suxh = 0.0f;
+        for (int64_t j = 0; j < N; ++j) {
+            const float u = ld32(dy, row + j, dt) * ld32(gamma, j, dt);
+            const float xh = (ld32(x, row + j, dt) - mu) * r;
+            const float uxh = u * xh;
+            su = su + u;
+            suxh = suxh + uxh;
+        }
+        const float mean_u = su / (float)N;
+        const float mean_uxh = suxh / (float)N;
+        for (int64_t j = 0; j < N; ++j) {
+            const float dyv = ld32(dy, row + j, dt);
+            const float u = dyv * ld32(gamma, j, dt);
+            const float xh = (ld32(x, row + j, dt) - mu) * r;
+            if (dx) {
+                const float a = u - mean_u;
+                const float b = xh * mean_uxh;
+                const float c = a - b;
+                store_elem(dx, row + j, dt, (double)(r * c));
+            }
+            const float g = dyv * xh;
+            ag[j] = ag[j] + g;
+            ab[j] = ab[j] + dyv;
+        }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+        if (dgamma) store_elem(dgamma, j, dt, (double)ag[j]);
+        if (dbeta) store_elem(dbeta, j, dt, (double)ab[j]);
+    }
+    free(ag);
+    free(ab);
+}

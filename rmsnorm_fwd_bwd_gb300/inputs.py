@@ -1,7 +1,7 @@
 """Seeded synthetic inputs and the workload table.
 
 This module is shared by the GPU tests, the oracle tests and the benchmark. It
-holds none of the RMSNorm arithmetic: it only draws random numbers and stores
+holds none of the RMSNorm or LayerNorm arithmetic: it only draws random numbers and stores
 them in the I/O dtype (round-to-nearest-even, done by numpy for float16 and by
 torch for bfloat16). It imports neither the GPU library nor the oracle.
 
@@ -14,6 +14,9 @@ Recipe (every tensor gets its own random stream):
   * adversarial rows: row i has class i mod 5 --
       0 all zero; 1 constant 1e4; 2 1e-20 * N(0,1);
       3 N(0,1) with one outlier 6e4 at column (i * 7919) mod N; 4 uniform[-1, 1).
+  * LayerNorm inputs: x = row_shift * s_i + x_scale * N(0,1), with one shift
+    s_i ~ N(0,1) per row (tag 5) so that rows have non-zero means;
+    gamma = 1 + 0.1 * N(0,1); beta = 0.1 * N(0,1) (tag 6); dy as above.
 
 Storage form (what the oracle and the GPU tests exchange): float32 data as
 np.float32, float16/bfloat16 as raw 16-bit patterns in np.uint16.
@@ -24,7 +27,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-TAG_X, TAG_GAMMA, TAG_DY, TAG_ADV_U, TAG_ADV_Z = 0, 1, 2, 3, 4
+TAG_X, TAG_GAMMA, TAG_DY, TAG_ADV_U, TAG_ADV_Z, TAG_SHIFT, TAG_BETA = 0, 1, 2, 3, 4, 5, 6
 ELEM_BYTES = {"float32": 4, "float16": 2, "bfloat16": 2}
 
 
@@ -40,20 +43,28 @@ class Workload:
     adversarial: bool = False
     seed: int = 0
     eps: float = 1e-6
+    op: str = "rmsnorm"          # or "layernorm"
+    row_shift: float = 0.0       # LayerNorm inputs: spread of the per-row means
 
     @property
     def elem_bytes(self) -> int:
         return ELEM_BYTES[self.dtype]
 
     def fwd_bytes(self) -> int:
-        """Algorithmic HBM bytes of one forward: read x, write y, read gamma, write rstd."""
+        """Algorithmic HBM bytes of one forward. RMSNorm: read x and gamma, write y
+        and rstd. LayerNorm: also read beta and write mean."""
         s = self.elem_bytes
+        if self.op == "layernorm":
+            return 2 * self.M * self.N * s + 2 * self.N * s + 8 * self.M
         return 2 * self.M * self.N * s + self.N * s + 4 * self.M
 
     def bwd_bytes(self) -> int:
         """Algorithmic HBM bytes of one backward: read x, dy, write dx, read gamma,
-        write dgamma, read rstd (the dgamma partials are overhead, not counted)."""
+        write dgamma, read rstd (the dgamma partials are overhead, not counted).
+        LayerNorm: also read mean and write dbeta."""
         s = self.elem_bytes
+        if self.op == "layernorm":
+            return 3 * self.M * self.N * s + 3 * self.N * s + 8 * self.M
         return 3 * self.M * self.N * s + 2 * self.N * s + 4 * self.M
 
 
@@ -68,6 +79,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("fp32_offset_16384x16384", 16384, 16384, "float32", offset=True),
     Workload("bf16_adversarial_8192x5120", 8192, 5120, "bfloat16", adversarial=True),
     Workload("bf16_adversarial_8192x4099", 8192, 4099, "bfloat16", adversarial=True),
+    Workload("ln_bf16_65536x4096", 65536, 4096, "bfloat16", eps=1e-5, op="layernorm", row_shift=2.0),
+    Workload("ln_fp32_16384x16384", 16384, 16384, "float32", eps=1e-5, op="layernorm", row_shift=2.0),
+    Workload("ln_bf16_16384x4099", 16384, 4099, "bfloat16", eps=1e-5, op="layernorm", row_shift=2.0),
 ]}
 
 HEADLINE = "bf16_65536x4096"
@@ -130,6 +144,21 @@ def make_inputs(M: int, N: int, dtype: str, *, seed: int = 0, offset: bool = Fal
     return to_storage(xf, dtype), to_storage(gf, dtype), to_storage(dyf, dtype)
 
 
+def make_ln_inputs(M: int, N: int, dtype: str, *, seed: int = 0, x_scale: float = 1.0,
+                   row_shift: float = 2.0, dy_scale: float = 1.0):
+    """LayerNorm inputs: storage-form ``x [M,N]``, ``gamma [N]``, ``beta [N]``, ``dy [M,N]``."""
+    xf = normal(seed, TAG_X, (M, N), x_scale)
+    if row_shift:
+        xf += normal(seed, TAG_SHIFT, (M, 1), row_shift)
+    gf = np.float32(1.0) + normal(seed, TAG_GAMMA, (N,), 0.1)
+    bf = normal(seed, TAG_BETA, (N,), 0.1)
+    dyf = normal(seed, TAG_DY, (M, N), dy_scale)
+    return to_storage(xf, dtype), to_storage(gf, dtype), to_storage(bf, dtype), to_storage(dyf, dtype)
+
+
 def workload_inputs(w: Workload):
+    if w.op == "layernorm":
+        return make_ln_inputs(w.M, w.N, w.dtype, seed=w.seed, x_scale=w.x_scale,
+                              row_shift=w.row_shift, dy_scale=w.dy_scale)
     return make_inputs(w.M, w.N, w.dtype, seed=w.seed, offset=w.offset,
                        x_scale=w.x_scale, dy_scale=w.dy_scale, adversarial=w.adversarial)
