@@ -1,4 +1,5 @@
-"""Python front end of ``librmsnorm.so`` (the C ABI in ``include/rmsnorm.h``).
+"""Python front end of ``librmsnorm.so`` (the C ABI in ``include/rmsnorm.h`` and
+``include/layernorm.h``).
 
 The functions named like the C entry points take the same arguments in the same
 order and only marshal them: a pointer argument may be a torch tensor (its
@@ -22,7 +23,8 @@ import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "librmsnorm.so")
-HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "rmsnorm.h")
+INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
+HEADER_PATH = os.path.join(INCLUDE_DIR, "rmsnorm.h")
 
 RMSNORM_F32, RMSNORM_F16, RMSNORM_BF16 = 0, 1, 2
 DTYPE_CODES = {"float32": RMSNORM_F32, "float16": RMSNORM_F16, "bfloat16": RMSNORM_BF16}
@@ -67,6 +69,9 @@ def _load():
             "rmsnorm_selftest_wait_timeout": (I, [ctypes.c_uint32, P]),
             "rmsnorm_fwd_strided": (I, [P, I64, P, P, I64, P, I64, I64, F, I, I, P]),
             "rmsnorm_bwd_strided": (I, [P, I64, P, I64, P, P, P, I64, P, I64, I64, I, I, P, SZ, P]),
+            "layernorm_fwd": (I, [P, I64, P, P, P, I64, P, P, I64, I64, F, I, P]),
+            "layernorm_bwd_workspace_size": (SZ, [I64, I64, I]),
+            "layernorm_bwd": (I, [P, I64, P, I64, P, P, P, P, I64, P, P, I64, I64, I, P, SZ, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -77,10 +82,15 @@ def _load():
 
 
 def header_functions() -> list:
-    """Names of the functions declared in include/rmsnorm.h."""
-    text = open(HEADER_PATH).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", text)))
+    """Names of the functions declared in include/*.h."""
+    names = set()
+    for fn in sorted(os.listdir(INCLUDE_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(INCLUDE_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b((?:rmsnorm|layernorm)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def _addr(p):
@@ -151,6 +161,24 @@ def rmsnorm_bwd_static_scratch(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, offs
     return _load().rmsnorm_bwd_static_scratch(_addr(dy), _addr(x), _addr(gamma), _addr(rstd),
                                               _addr(dx), _addr(dgamma), int(M), int(N),
                                               _dtype_code(dtype), int(offset), _stream(stream))
+
+
+def layernorm_fwd(x, ldx, gamma, beta, y, ldy, mean, rstd, M, N, eps, dtype, stream=None) -> int:
+    return _load().layernorm_fwd(_addr(x), int(ldx), _addr(gamma), _addr(beta), _addr(y), int(ldy),
+                                 _addr(mean), _addr(rstd), int(M), int(N), float(eps), _dtype_code(dtype),
+                                 _stream(stream))
+
+
+def layernorm_bwd_workspace_size(M, N, dtype) -> int:
+    return int(_load().layernorm_bwd_workspace_size(int(M), int(N), _dtype_code(dtype)))
+
+
+def layernorm_bwd(dy, lddy, x, ldx, gamma, mean, rstd, dx, lddx, dgamma, dbeta, M, N, dtype, workspace,
+                  workspace_bytes, stream=None) -> int:
+    return _load().layernorm_bwd(_addr(dy), int(lddy), _addr(x), int(ldx), _addr(gamma), _addr(mean),
+                                 _addr(rstd), _addr(dx), int(lddx), _addr(dgamma), _addr(dbeta), int(M),
+                                 int(N), _dtype_code(dtype), _addr(workspace), int(workspace_bytes),
+                                 _stream(stream))
 
 
 def rmsnorm_status_string(status: int) -> str:

@@ -1,6 +1,10 @@
-// api.cu -- the C ABI declared in include/rmsnorm.h: argument validation, launch
-// planning (path, cluster size, threads, pipeline depth, persistent grid size
-// from the device's SM count and occupancy) and kernel launches.
+// api.cu -- the C ABI declared in include/rmsnorm.h and include/layernorm.h:
+// argument validation, launch planning (path, cluster size, threads, pipeline
+// depth, persistent grid size from the device's SM count and occupancy) and
+// kernel launches.
+//
+// Passes: 0 RMSNorm forward, 1 RMSNorm backward, 2 LayerNorm forward,
+// 3 LayerNorm backward. Odd passes are backward passes (two input streams).
 //
 // Argument contract (page "Check an AI model calculation before accelerating
 // it", section "The memory contract is part of the computation"): inputs are
@@ -15,6 +19,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "../../include/layernorm.h"
 #include "../../include/rmsnorm.h"
 #include "launch.h"
 
@@ -34,7 +39,9 @@ constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per te
 //    latency-bound. The forward keeps 2 stages; the backward 2-4.
 constexpr int kMinVpt = 2;
 constexpr int kThreadCap[2] = {256, 128};  // forward, backward (no cluster)
-constexpr int kMaxElemsPerThread = 32;     // backward: keeps x, u and dgamma sums in registers
+// backward: elements a thread keeps in registers (x, u and dgamma sums; LayerNorm
+// also dbeta sums)
+constexpr int kMaxElemsPerThread[2] = {32, 16};  // RMSNorm, LayerNorm
 constexpr int kRingPerSm[2] = {48 << 10, 96 << 10};
 constexpr int kMaxBlocksPerSm = 16;
 // Rows split over a cluster pay a cluster barrier per row; there a third
@@ -59,7 +66,8 @@ struct Override {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
-Override g_override[2];
+constexpr int kPasses = 4;
+Override g_override[kPasses];
 unsigned g_override_gen = 0;
 std::map<std::tuple<int, int, int64_t, int, int, int, int, unsigned>, Plan> g_plans;
 std::map<std::pair<const void*, int>, bool> g_attr_done;
@@ -67,6 +75,16 @@ std::map<std::pair<const void*, int>, bool> g_attr_done;
 int elem_bytes(int dt) { return dt == RMSNORM_F32 ? 4 : 2; }
 int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+const void* kernel_for(int pass, const Plan& p) {
+    switch (pass) {
+    case 0: return fwd_kernel(p);
+    case 1: return bwd_kernel(p);
+    case 2: return ln_fwd_kernel(p);
+    case 3: return ln_bwd_kernel(p);
+    default: return nullptr;
+    }
+}
 
 // Caller holds g_mu.
 bool device_info(int dev, DeviceInfo*& out) {
@@ -136,6 +154,8 @@ bool occupancy_units(const void* k, const Plan& p, const DeviceInfo& di, int cap
 // TMA path: rows whose byte length is a multiple of 16, split over a cluster so
 // that one CTA stages at most kSliceMaxBytes per tensor.
 bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    const int dir = pass & 1;     // 0 forward, 1 backward
+    const int ln = pass >> 1;     // 0 RMSNorm, 1 LayerNorm
     const int s = elem_bytes(dt);
     const int vec = 16 / s;
     if ((static_cast<int64_t>(N) * s) % 16 != 0) return false;
@@ -146,12 +166,12 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kThreadCap[pass]);
+        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[dir] : kThreadCap[dir]);
         for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
-        if (pass == 1 && cl == 1)
-            while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread &&
+        if (dir == 1 && cl == 1)
+            while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread[ln] &&
                    round_up(ceil_div(nvec, vpt / 2), 32) <= kTmaMaxThreads)
                 vpt /= 2;  // more threads rather than more registers
         while (vpt > 1 && ceil_div(nvec, vpt / 2) <= 32) vpt /= 2;  // tiny rows: one warp
@@ -163,16 +183,19 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
     if (cl > 8) return false;
     const int slice = (N / cl) * s;
-    const int stage = (pass == 0 ? 1 : 2) * slice;
-    // mbarriers, warp partials, abort flag (+ the backward's fp32 gamma slice)
-    const int fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : (N / cl) * 4);
+    const int stage = (dir == 0 ? 1 : 2) * slice;
+    // warp partials [2][k][32] floats (k = 1 RMSNorm, 3 LayerNorm forward, 2
+    // LayerNorm backward), abort flag (+ the backward's fp32 gamma slice); the
+    // mbarriers are counted per stage below
+    const int partials = pass == 2 ? 3 : (pass == 3 ? 2 : 1);
+    const int fixed = 2 * partials * 32 * 4 + 16 + (dir == 0 ? 0 : (N / cl) * 4);
     // ring shape: blocks per SM and stages aiming at kRingPerSm resident per SM
     int bps = ov.blocks_per_sm;
     int stages = ov.stages;
     if (cl > 1) {
-        if (!stages) stages = kClusterStages[pass];
-        if (!bps) bps = kClusterBlocksPerSm[pass];
-    } else if (pass == 0) {
+        if (!stages) stages = kClusterStages[dir];
+        if (!bps) bps = kClusterBlocksPerSm[dir];
+    } else if (dir == 0) {
         if (!stages) stages = 2;
         if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[0], 2 * stage), 2),
                                                            kMaxBlocksPerSm));
@@ -192,7 +215,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     p.per_thread = vpt;
     p.stages = stages;
     p.smem = static_cast<size_t>(stages) * (stage + 8) + fixed;
-    const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
+    const void* k = kernel_for(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
     if (!occupancy_units(k, p, di, bps, units)) return false;
@@ -211,14 +234,17 @@ bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.threads = threads;
     p.per_thread = 0;
     p.stages = 0;
-    p.smem = pass == 0 ? 0 : static_cast<size_t>(N) * 4;
-    const void* k = pass == 0 ? fwd_kernel(p) : bwd_kernel(p);
+    // backward: fp32 column accumulators, one plane per reduced gradient
+    const int planes = pass == 1 ? 1 : (pass == 3 ? 2 : 0);
+    p.smem = static_cast<size_t>(planes) * N * 4;
+    const void* k = kernel_for(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
     if (!occupancy_units(k, p, di, 0, units)) return false;
-    if (pass == 1) {
-        // keep the dgamma partials (units x N floats) within kScalarWorkspaceCap
-        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
+    if (planes) {
+        // keep the partials (planes x units x N floats) within kScalarWorkspaceCap
+        const int64_t cap =
+            std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(planes) * N));
         if (units > cap) units = cap;
     }
     p.units = units < M ? units : M;
@@ -270,7 +296,7 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
     if (layout == kLayoutAligned && tma_shape) path = kPathTma;
-    else if (layout != kLayoutMixed) path = kPathRowVec;
+    else if (layout != kLayoutMixed && pass < 2) path = kPathRowVec;  // LayerNorm: no row-vector kernels
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
@@ -428,6 +454,100 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     return RMSNORM_OK;
 }
 
+rmsnorm_status ln_fwd_impl(const void* x, int64_t ldx, const void* gamma, const void* beta, void* y, int64_t ldy,
+                           float* mean, float* rstd, int64_t M, int64_t N, float eps, rmsnorm_dtype dtype,
+                           rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, 0);
+    if (st != RMSNORM_OK) return st;
+    if (!std::isfinite(eps) || !(eps > 0.0f)) return RMSNORM_ERR_EPS;
+    const size_t s = elem_bytes(dtype);
+    if (!pitch_ok(ldx, N, M, s) || !pitch_ok(ldy, N, M, s)) return RMSNORM_ERR_SHAPE;
+    if (M == 0) return RMSNORM_OK;
+    if (!x || !gamma || !beta || !y) return RMSNORM_ERR_NULL;
+    if (!aligned(x, s) || !aligned(gamma, s) || !aligned(beta, s) || !aligned(y, s) || !aligned(mean, 4) ||
+        !aligned(rstd, 4))
+        return RMSNORM_ERR_ALIGN;
+    // TMA path: 16-byte aligned rows; anything else: the general path
+    const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(beta, 16) && aligned(y, 16) &&
+                     (ldx * s) % 16 == 0 && (ldy * s) % 16 == 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(2, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
+        return RMSNORM_ERR_UNSUPPORTED;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.y = y;
+    a.mean_out = mean;
+    a.rstd_out = rstd;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.ldx = ldx;
+    a.ldy = ldy;
+    a.eps = eps;
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_rows(kernel_for(2, p), p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx, const void* gamma,
+                           const float* mean, const float* rstd, void* dx, int64_t lddx, void* dgamma, void* dbeta,
+                           int64_t M, int64_t N, rmsnorm_dtype dtype, void* workspace, size_t workspace_bytes,
+                           rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, 0);
+    if (st != RMSNORM_OK) return st;
+    const size_t s = elem_bytes(dtype);
+    if (!pitch_ok(ldx, N, M, s) || !pitch_ok(lddy, N, M, s) || !pitch_ok(lddx, N, M, s)) return RMSNORM_ERR_SHAPE;
+    if (!dgamma || !dbeta) return RMSNORM_ERR_NULL;
+    if (!aligned(dgamma, s) || !aligned(dbeta, s)) return RMSNORM_ERR_ALIGN;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (M == 0) {
+        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs, dbeta) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
+    if (!dy || !x || !gamma || !mean || !rstd || !dx || !workspace) return RMSNORM_ERR_NULL;
+    if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(mean, 4) ||
+        !aligned(rstd, 4) || !aligned(workspace, 16))
+        return RMSNORM_ERR_ALIGN;
+    const bool a16 = aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16) &&
+                     (ldx * s) % 16 == 0 && (lddy * s) % 16 == 0 && (lddx * s) % 16 == 0;
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(3, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
+        return RMSNORM_ERR_UNSUPPORTED;
+    const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.dy = dy;
+    a.mean_in = mean;
+    a.rstd_in = rstd;
+    a.dx = dx;
+    a.ws = static_cast<float*>(workspace);
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.ldx = ldx;
+    a.lddy = lddy;
+    a.lddx = lddx;
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_rows(kernel_for(3, p), p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs, dbeta) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
 }  // namespace
 }  // namespace rmsnorm
 
@@ -474,6 +594,33 @@ extern "C" rmsnorm_status rmsnorm_bwd_strided(const void* dy, int64_t lddy, cons
                     workspace_bytes, stream);
 }
 
+extern "C" rmsnorm_status layernorm_fwd(const void* x, int64_t ldx, const void* gamma, const void* beta, void* y,
+                                        int64_t ldy, float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                                        rmsnorm_dtype dtype, rmsnorm_stream_t stream) {
+    return ln_fwd_impl(x, ldx, gamma, beta, y, ldy, mean, rstd, M, N, eps, dtype, stream);
+}
+
+extern "C" size_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype) {
+    if (check_common(M, N, dtype, 0) != RMSNORM_OK || M == 0) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (current_device(dev, di) != RMSNORM_OK) return 0;
+    int64_t units = 0;
+    Plan p;
+    for (int layout : {kLayoutMixed, kLayoutAligned})
+        if (get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p) && p.units > units) units = p.units;
+    return 2 * static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+}
+
+extern "C" rmsnorm_status layernorm_bwd(const void* dy, int64_t lddy, const void* x, int64_t ldx, const void* gamma,
+                                        const float* mean, const float* rstd, void* dx, int64_t lddx, void* dgamma,
+                                        void* dbeta, int64_t M, int64_t N, rmsnorm_dtype dtype, void* workspace,
+                                        size_t workspace_bytes, rmsnorm_stream_t stream) {
+    return ln_bwd_impl(dy, lddy, x, ldx, gamma, mean, rstd, dx, lddx, dgamma, dbeta, M, N, dtype, workspace,
+                       workspace_bytes, stream);
+}
+
 extern "C" const char* rmsnorm_status_string(rmsnorm_status status) {
     switch (status) {
     case RMSNORM_OK: return "ok";
@@ -503,7 +650,7 @@ extern "C" rmsnorm_status rmsnorm_device_error(uint32_t* flags, int clear) {
 
 extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,
                                                 int aligned16, char* buf, size_t buf_len) {
-    if (pass != 0 && pass != 1) return RMSNORM_ERR_ARG;
+    if (pass < 0 || pass >= kPasses) return RMSNORM_ERR_ARG;
     rmsnorm_status st = check_common(M, N, dtype, 0);
     if (st != RMSNORM_OK) return st;
     if (!buf || buf_len == 0) return RMSNORM_ERR_NULL;
@@ -529,7 +676,7 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
 
 extern "C" rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int stages,
                                                       int blocks_per_sm) {
-    if (pass != 0 && pass != 1) return RMSNORM_ERR_ARG;
+    if (pass < 0 || pass >= kPasses) return RMSNORM_ERR_ARG;
     if (threads < 0 || threads > 1024 || threads % 32 != 0 || stages < 0 || stages > 64 || blocks_per_sm < 0 ||
         (vpt != 0 && vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8))
         return RMSNORM_ERR_ARG;

@@ -290,14 +290,17 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 // ry, ry + 32, ... in sequence (8 threads read 128 contiguous bytes of a row);
 // then thread cq adds the 32 row-lane sums in ry order. units == 0 (no rows)
 // writes zeros. Rows of N % 4 != 0 floats are read one column at a time.
+// blockIdx.y = 1 sums the second plane (LayerNorm's dbeta partials) into out1.
 template <int DT>
 __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
-                                                           void* dgamma) {
+                                                           void* out0, void* out1) {
     using E = Elem<DT>;
     __shared__ float4 part[32][8];
     const int cq = threadIdx.x & 7;
     const int ry = threadIdx.x >> 3;
     const int col = blockIdx.x * 32 + cq * 4;
+    void* dgamma = blockIdx.y == 0 ? out0 : out1;
+    if (blockIdx.y != 0) ws += units * static_cast<int64_t>(N);
     griddep_wait();  // the partial sums come from the row kernel just before
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if ((N & 3) == 0) {
@@ -382,6 +385,10 @@ const void* dgamma_reduce_kernel_ptr(int dtype) {
 cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
     const void* k = bwd_kernel(p);
     if (!k) return cudaErrorInvalidDeviceFunction;
+    return launch_rows(k, p, a, s);
+}
+
+cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
@@ -406,11 +413,11 @@ cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, void* dbeta) {
     const void* k = dgamma_reduce_kernel_ptr(dtype);
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), dbeta ? 2u : 1u, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -419,7 +426,7 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma};
+    void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma, &dbeta};
     return cudaLaunchKernelExC(&cfg, k, params);
 }
 

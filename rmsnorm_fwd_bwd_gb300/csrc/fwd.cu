@@ -270,27 +270,7 @@ const void* fwd_kernel(const Plan& p) {
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
     const void* k = fwd_kernel(p);
     if (!k) return cudaErrorInvalidDeviceFunction;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    if (p.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs += 1;
-    RowArgs args = a;
-    void* params[] = {&args};
-    return cudaLaunchKernelExC(&cfg, k, params);
+    return launch_rows(k, p, a, s);
 }
 
 }  // namespace rmsnorm

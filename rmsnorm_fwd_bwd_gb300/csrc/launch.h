@@ -17,7 +17,10 @@ struct RowArgs {
     void* y;               // forward output
     float* rstd_out;       // forward output
     void* dx;              // backward output
-    float* ws;             // backward: dgamma partials [units][N]
+    float* ws;             // backward: dgamma partials [units][N] (LayerNorm: then dbeta partials)
+    const void* beta;      // LayerNorm forward
+    float* mean_out;       // LayerNorm forward output (may be null, as may rstd_out there)
+    const float* mean_in;  // LayerNorm backward: saved mean per row
     int64_t M;
     int N;
     int64_t ldx, ldy, lddy, lddx;  // row pitches in elements (>= N)
@@ -54,12 +57,19 @@ struct Plan {
 const void* fwd_kernel(const Plan& p);
 const void* bwd_kernel(const Plan& p);
 const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backward
+const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
+const void* ln_bwd_kernel(const Plan& p);
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s);
+// Launch `k` with the plan's grid, block, shared memory and cluster shape, and
+// programmatic stream serialization.
+cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s);
+// Column sums of the partial rows: dgamma from plane 0 of ws and, when dbeta is
+// not null, dbeta from plane 1 (planes of units x N floats, one after the other).
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
-                                 cudaStream_t s);
+                                 cudaStream_t s, void* dbeta = nullptr);
 
 // Device address of the error word on the current device (nullptr on failure).
 uint32_t* device_error_word();

@@ -93,3 +93,66 @@ def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, st
         dx = B.to_numpy(dxt, dtype).reshape(M, N)
         dg = B.to_numpy(dgt, dtype)
     return yo, ro, dx, dg
+
+
+def ln_run(x, g, b, dy, dtype, eps=1e-5, misalign=False, do_bwd=True, stats=True, stream=None):
+    """LayerNorm forward (and backward) through the C ABI, dense rows. Returns
+    numpy storage arrays (y, mean, rstd, dx, dgamma, dbeta); mean and rstd are
+    None when ``stats`` is False (the forward is then called with NULL for
+    them), the gradients None when ``do_bwd`` is False.
+
+    misalign: False, True, or a set of names among {"x", "g", "b", "dy", "y", "dx"}."""
+    torch = _torch()
+    M, N = x.shape
+    names = {"x", "g", "b", "dy", "y", "dx"} if misalign is True else set(misalign or ())
+    keep = []
+    _, xt = _place(x, dtype, "x" in names); keep.append(_)
+    _, gt = _place(g, dtype, "g" in names); keep.append(_)
+    _, bt = _place(b, dtype, "b" in names); keep.append(_)
+    _, dyt = _place(dy, dtype, "dy" in names); keep.append(_)
+
+    def out(n, name):
+        buf, view = _guarded(n, dtype)
+        if name in names:
+            b2 = torch.empty(n + 2 * GUARD + 1, dtype=view.dtype, device=view.device)
+            b2[1:] = buf
+            buf, view = b2[1:], b2[1 + GUARD:1 + GUARD + n]
+        return buf, view
+
+    ybuf, y = out(M * N, "y")
+    mbuf, mean = _guarded(M, "float32")
+    rbuf, rstd = _guarded(M, "float32")
+    st = B.layernorm_fwd(xt, N, gt, bt, y, N, mean if stats else None, rstd if stats else None, M, N, eps,
+                         dtype, stream)
+    assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+    res = [None] * 6
+    if do_bwd:
+        if not stats:
+            raise ValueError("the backward needs the saved statistics")
+        dxbuf, dxt = out(M * N, "dx")
+        dgbuf, dgt = _guarded(N, dtype)
+        dbbuf, dbt = _guarded(N, dtype)
+        wsz = B.layernorm_bwd_workspace_size(M, N, dtype)
+        ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device="cuda")
+        st = B.layernorm_bwd(dyt, N, xt, N, gt, mean, rstd, dxt, N, dgt, dbt, M, N, dtype, ws, wsz, stream)
+        assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+    torch.cuda.synchronize()
+    assert _guards_intact(ybuf, dtype), "forward wrote outside y"
+    assert _guards_intact(mbuf, "float32"), "forward wrote outside mean"
+    assert _guards_intact(rbuf, "float32"), "forward wrote outside rstd"
+    res[0] = B.to_numpy(y, dtype).reshape(M, N)
+    if stats:
+        res[1] = B.to_numpy(mean, "float32")
+        res[2] = B.to_numpy(rstd, "float32")
+    else:
+        sent = np.uint32(SENTINEL["float32"]).view(np.float32)
+        assert np.all(B.to_numpy(mean, "float32") == sent) and np.all(B.to_numpy(rstd, "float32") == sent), \
+            "forward wrote mean/rstd although they were NULL"
+    if do_bwd:
+        assert _guards_intact(dxbuf, dtype), "backward wrote outside dx"
+        assert _guards_intact(dgbuf, dtype), "backward wrote outside dgamma"
+        assert _guards_intact(dbbuf, dtype), "backward wrote outside dbeta"
+        res[3] = B.to_numpy(dxt, dtype).reshape(M, N)
+        res[4] = B.to_numpy(dgt, dtype)
+        res[5] = B.to_numpy(dbt, dtype)
+    return tuple(res)

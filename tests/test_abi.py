@@ -62,10 +62,33 @@ def test_host_validation_without_gpu():
     assert B.rmsnorm_bwd_workspace_size(0, 8, 0) == 0
     assert B.rmsnorm_bwd_workspace_size(4, 0, 0) == 0
     assert B.rmsnorm_bwd_workspace_size(4, 8, 9) == 0
-    assert B.rmsnorm_set_launch_override(2, 0, 0, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(4, 0, 0, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(-1, 0, 0, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(3, 0, 0, 0, 0) == 0
     assert B.rmsnorm_set_launch_override(0, 33, 0, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(0, 0, 3, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(0, 0, 0, 0, 0) == 0
+
+
+def test_layernorm_host_validation_without_gpu():
+    # layernorm_fwd(x, ldx, gamma, beta, y, ldy, mean, rstd, M, N, eps, dtype, stream)
+    assert B.layernorm_fwd(None, 8, None, None, None, 8, None, None, 4, 8, 1e-5, 5, 0) == 3
+    assert B.layernorm_fwd(None, 8, None, None, None, 8, None, None, 4, 0, 1e-5, 0, 0) == 2
+    assert B.layernorm_fwd(None, 7, None, None, None, 8, None, None, 4, 8, 1e-5, 0, 0) == 2  # ldx < N
+    assert B.layernorm_fwd(None, 8, None, None, None, 8, None, None, 4, 8, 0.0, 0, 0) == 4
+    assert B.layernorm_fwd(None, 8, None, None, None, 8, None, None, 0, 8, 1e-5, 0, 0) == 0  # M == 0
+    assert B.layernorm_fwd(0x1000, 8, 0x1000, None, 0x2000, 8, None, None, 4, 8, 1e-5, 0, 0) == 1
+    assert B.layernorm_fwd(0x1000, 8, 0x1000, 0x1002, 0x2000, 8, None, None, 4, 8, 1e-5, 0, 0) == 5
+    assert B.layernorm_fwd(0x1000, 8, 0x1000, 0x1000, 0x2000, 8, 0x3002, None, 4, 8, 1e-5, 0, 0) == 5
+    # layernorm_bwd(dy, lddy, x, ldx, gamma, mean, rstd, dx, lddx, dgamma, dbeta, M, N, dtype, ws, bytes, stream)
+    assert B.layernorm_bwd(None, 8, None, 8, None, None, None, None, 8, 0x1000, None, 4, 8, 0, None, 0, 0) == 1
+    assert B.layernorm_bwd(None, 8, None, 8, None, None, None, None, 8, 0x1000, 0x1001, 4, 8, 1, None, 0, 0) == 5
+    assert B.layernorm_bwd(None, 8, None, 8, None, None, None, None, 8, 0x1000, 0x2000, 4, 8, 0, None, 0, 0) == 1
+    assert B.layernorm_bwd(0x1000, 8, 0x1000, 8, 0x1000, 0x1000, 0x1000, 0x1000, 8, 0x1000, 0x2000, 4, 8, 0,
+                           0x1008, 1 << 20, 0) == 5
+    assert B.layernorm_bwd(None, 8, None, 9, None, None, None, None, 8, 0x1000, 0x2000, 4, 10, 0, None, 0, 0) == 2
+    assert B.layernorm_bwd_workspace_size(0, 8, 0) == 0
+    assert B.layernorm_bwd_workspace_size(4, 8, 9) == 0
 
 
 def test_library_is_in_tree_and_built_for_sm_103a():
