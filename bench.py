@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark: RMSNorm forward + backward HBM throughput on GB300.
+"""Benchmark: RMSNorm (and LayerNorm) forward + backward HBM throughput on GB300.
 
 One step = one forward (rmsnorm_fwd) and one backward (rmsnorm_bwd: fused row
 kernel + dgamma column reduction) over the whole workload, inputs resident in
@@ -18,6 +18,10 @@ roofline = the backward pass (the dominant cost) against the measured HBM copy
          bandwidth in MEASURED_PEAKS.json.
 cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
          fp32-intermediate reference) on a bounded row sample of the workload.
+
+--workload ln_*: the same step for LayerNorm (layernorm_fwd + layernorm_bwd:
+         fused row kernel + dgamma/dbeta column reduction); its algorithmic
+         bytes add beta and dbeta (N*s each) and the saved mean (4*M each way).
 
 Multi-GPU (torchrun): one process per GPU, each running an independent replica
 of the workload (weak scaling); there is no collective on the data path.
@@ -40,6 +44,95 @@ if ROOT not in sys.path:
 
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RMSNorm fwd/bwd HBM GB/s & % of peak, bf16 M=65536 N=4096, 1 GB300"
+
+
+def metric_for(w) -> str:
+    if w.op == "layernorm":
+        return f"LayerNorm fwd/bwd HBM GB/s & % of peak, {w.dtype} M={w.M} N={w.N}, 1 GB300"
+    return METRIC
+
+
+# --------------------------------------------------------------------------- #
+# the two operations behind one interface
+# --------------------------------------------------------------------------- #
+class RmsOp:
+    """RMSNorm: inputs x, g, dy; outputs y, r (rstd), dx, dg."""
+    name = "rmsnorm"
+    inputs = ("x", "g", "dy")
+    outputs = ("y", "r", "dx", "dg")
+    passes = (0, 1)
+    kernel = "rmsnorm_bwd (fused row kernel + dgamma reduce)"
+
+    def __init__(self, w):
+        self.w = w
+
+    def host_inputs(self):
+        from rmsnorm_fwd_bwd_gb300 import inputs
+        x, g, dy = inputs.workload_inputs(self.w)
+        return {"x": x, "g": g, "dy": dy}
+
+    def workspace_size(self, B):
+        return B.rmsnorm_bwd_workspace_size(self.w.M, self.w.N, self.w.dtype)
+
+    def fwd(self, B, b, s):
+        w = self.w
+        return B.rmsnorm_fwd(b["x"], b["g"], b["y"], b["r"], w.M, w.N, w.eps, w.dtype, int(w.offset), s)
+
+    def bwd(self, B, b, s, wsz):
+        w = self.w
+        return B.rmsnorm_bwd(b["dy"], b["x"], b["g"], b["r"], b["dx"], b["dg"], w.M, w.N, w.dtype,
+                             int(w.offset), b["ws"], wsz, s)
+
+    def oracle_step(self, orc, h, a, rows):
+        w = self.w
+        x, dy = h["x"][a:a + rows], h["dy"][a:a + rows]
+        orc.fwd_reference(x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
+        orc.bwd_reference(dy, x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
+
+    def step_bytes(self, rows):
+        s, N = self.w.elem_bytes, self.w.N
+        return (2 * rows * N * s + N * s + 4 * rows) + (3 * rows * N * s + 2 * N * s + 4 * rows)
+
+
+class LnOp(RmsOp):
+    """LayerNorm: inputs x, g, b, dy; outputs y, m (mean), r (rstd), dx, dg, db."""
+    name = "layernorm"
+    inputs = ("x", "g", "b", "dy")
+    outputs = ("y", "m", "r", "dx", "dg", "db")
+    passes = (2, 3)
+    kernel = "layernorm_bwd (fused row kernel + dgamma/dbeta reduce)"
+
+    def host_inputs(self):
+        from rmsnorm_fwd_bwd_gb300 import inputs
+        x, g, b, dy = inputs.workload_inputs(self.w)
+        return {"x": x, "g": g, "b": b, "dy": dy}
+
+    def workspace_size(self, B):
+        return B.layernorm_bwd_workspace_size(self.w.M, self.w.N, self.w.dtype)
+
+    def fwd(self, B, b, s):
+        w = self.w
+        return B.layernorm_fwd(b["x"], w.N, b["g"], b["b"], b["y"], w.N, b["m"], b["r"], w.M, w.N, w.eps,
+                               w.dtype, s)
+
+    def bwd(self, B, b, s, wsz):
+        w = self.w
+        return B.layernorm_bwd(b["dy"], w.N, b["x"], w.N, b["g"], b["m"], b["r"], b["dx"], w.N, b["dg"],
+                               b["db"], w.M, w.N, w.dtype, b["ws"], wsz, s)
+
+    def oracle_step(self, orc, h, a, rows):
+        w = self.w
+        x, dy = h["x"][a:a + rows], h["dy"][a:a + rows]
+        orc.ln_fwd_reference(x, h["g"], h["b"], w.dtype, eps=w.eps)
+        orc.ln_bwd_reference(dy, x, h["g"], w.dtype, eps=w.eps)
+
+    def step_bytes(self, rows):
+        s, N = self.w.elem_bytes, self.w.N
+        return (2 * rows * N * s + 2 * N * s + 8 * rows) + (3 * rows * N * s + 3 * N * s + 8 * rows)
+
+
+def op_for(w):
+    return LnOp(w) if w.op == "layernorm" else RmsOp(w)
 
 
 # --------------------------------------------------------------------------- #
@@ -165,25 +258,23 @@ def recorded_traffic(kernel_key: str):
     return rec.get("dram_bytes_per_launch")
 
 
-def cpu_oracle_rate(w, x, g, dy, budget_s: float):
+def cpu_oracle_rate(w, h, budget_s: float):
     """Time the oracle's fp32-intermediate reference (fwd + bwd) on a row sample sized
-    to about budget_s seconds. Returns (GB/s of algorithmic bytes, rows, seconds)."""
+    to about budget_s seconds. h: the workload's host inputs. Returns (GB/s of
+    algorithmic bytes, rows, seconds)."""
     from oracle import oracle as orc
-    s = w.elem_bytes
+    op = op_for(w)
 
     def run(rows):
-        xs, dys = x[:rows], dy[:rows]
         t = time.perf_counter()
-        orc.fwd_reference(xs, g, w.dtype, eps=w.eps, offset=w.offset)
-        orc.bwd_reference(dys, xs, g, w.dtype, eps=w.eps, offset=w.offset)
+        op.oracle_step(orc, h, 0, rows)
         return time.perf_counter() - t
 
     probe = min(64, w.M)
     t = run(probe)
     rows = int(min(w.M, max(probe, probe * budget_s / max(t, 1e-6))))
     t = run(rows)
-    nbytes = (2 * rows * w.N * s + w.N * s + 4 * rows) + (3 * rows * w.N * s + 2 * w.N * s + 4 * rows)
-    return nbytes / t / 1e9, rows, t
+    return op.step_bytes(rows) / t / 1e9, rows, t
 
 
 # --------------------------------------------------------------------------- #
@@ -194,33 +285,26 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     from oracle import oracle as orc
-    from rmsnorm_fwd_bwd_gb300 import inputs
-    x, g, dy = inputs.workload_inputs(w)
+    op = op_for(w)
+    h = op.host_inputs()
     orc.build()
-    s = w.elem_bytes
     total_budget = 60.0
     probe = 64
     t0 = time.perf_counter()
-    orc.fwd_reference(x[:probe], g, w.dtype, eps=w.eps, offset=w.offset)
-    orc.bwd_reference(dy[:probe], x[:probe], g, w.dtype, eps=w.eps, offset=w.offset)
+    op.oracle_step(orc, h, 0, probe)
     per_row = (time.perf_counter() - t0) / probe
     rows = int(max(1, min(w.M, total_budget / max(args.steps + args.warmup, 1) / max(per_row, 1e-9))))
     starts = [(i * rows) % max(1, w.M - rows + 1) for i in range(args.steps + args.warmup)]
     for i in range(args.warmup):
-        a = starts[i]
-        orc.fwd_reference(x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
-        orc.bwd_reference(dy[a:a + rows], x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+        op.oracle_step(orc, h, starts[i], rows)
     t0 = time.perf_counter()
     for i in range(args.warmup, args.warmup + args.steps):
-        a = starts[i]
-        orc.fwd_reference(x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
-        orc.bwd_reference(dy[a:a + rows], x[a:a + rows], g, w.dtype, eps=w.eps, offset=w.offset)
+        op.oracle_step(orc, h, starts[i], rows)
     dt = time.perf_counter() - t0
-    nbytes = (2 * rows * w.N * s + w.N * s + 4 * rows) + (3 * rows * w.N * s + 2 * w.N * s + 4 * rows)
-    value = nbytes * args.steps / dt / 1e9
+    value = op.step_bytes(rows) * args.steps / dt / 1e9
     sample = f"{rows} consecutive rows of the {w.M}x{w.N} workload per step"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(w),
@@ -234,7 +318,8 @@ def run_reference(args, w):
 
 
 def workload_config(w):
-    return {"workload": f"RMSNorm fwd+bwd {w.dtype} M={w.M} N={w.N} eps={w.eps:g}"
+    title = "LayerNorm" if w.op == "layernorm" else "RMSNorm"
+    return {"workload": f"{title} fwd+bwd {w.dtype} M={w.M} N={w.N} eps={w.eps:g}"
                         + (" offset" if w.offset else ""),
             "name": w.name, "M": w.M, "N": w.N, "io_dtype": w.dtype, "offset": w.offset,
             "l2": "inputs larger than L2 (no flush)" if w.M * w.N * w.elem_bytes > 129e6
@@ -246,45 +331,50 @@ def workload_config(w):
 # our arm
 # --------------------------------------------------------------------------- #
 def run_ours(args, w):
-    import numpy as np
     import torch
     from rmsnorm_fwd_bwd_gb300 import binding as B
-    from rmsnorm_fwd_bwd_gb300 import inputs
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
+    op = op_for(w)
     dt = w.dtype
     M, N = w.M, w.N
 
-    x_np, g_np, dy_np = inputs.workload_inputs(w)
-    x_h = B.to_device(x_np.reshape(-1), dt, "cpu").pin_memory()
-    g_h = B.to_device(g_np, dt, "cpu").pin_memory()
-    dy_h = B.to_device(dy_np.reshape(-1), dt, "cpu").pin_memory()
-    x = x_h.to(dev).view(M, N)
-    g = g_h.to(dev)
-    dy = dy_h.to(dev).view(M, N)
-    y = torch.empty_like(x)
-    dx = torch.empty_like(x)
-    dg = torch.empty_like(g)
-    rstd = torch.empty(M, dtype=torch.float32, device=dev)
-    wsz = B.rmsnorm_bwd_workspace_size(M, N, dt)
-    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+    h_np = op.host_inputs()
+    # pinned host copies of the inputs (the end-to-end leg copies them in every step)
+    host = {k: B.to_device(v.reshape(-1), dt, "cpu").pin_memory() for k, v in h_np.items()}
+    wsz = op.workspace_size(B)
+
+    def device_set():
+        b = {k: v.to(dev) for k, v in host.items()}
+        b["y"] = torch.empty_like(b["x"])
+        b["dx"] = torch.empty_like(b["x"])
+        b["dg"] = torch.empty_like(b["g"])
+        if "db" in op.outputs:
+            b["db"] = torch.empty_like(b["g"])
+        for k in ("m", "r"):
+            if k in op.outputs:
+                b[k] = torch.empty(M, dtype=torch.float32, device=dev)
+        b["ws"] = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+        return b
+
+    bufs = device_set()
     flush = None
     if M * N * w.elem_bytes < 256e6:
         flush = torch.empty(int(512e6), dtype=torch.uint8, device=dev)
 
     def fwd():
-        st = B.rmsnorm_fwd(x, g, y, rstd, M, N, w.eps, dt, int(w.offset), stream)
+        st = op.fwd(B, bufs, stream)
         if st:
-            raise B.RMSNormError(st, "rmsnorm_fwd")
+            raise B.RMSNormError(st, f"{op.name} forward")
 
     def bwd():
-        st = B.rmsnorm_bwd(dy, x, g, rstd, dx, dg, M, N, dt, int(w.offset), ws, wsz, stream)
+        st = op.bwd(B, bufs, stream, wsz)
         if st:
-            raise B.RMSNormError(st, "rmsnorm_bwd")
+            raise B.RMSNormError(st, f"{op.name} backward")
 
     B.rmsnorm_device_error(clear=True)
     for _ in range(args.warmup):
@@ -331,27 +421,21 @@ def run_ours(args, w):
     # duplex); the timed region covers all steps on both streams.
     e2e_steps = max(3, min(K, args.e2e_steps))
     streams = [stream, torch.cuda.Stream(dev)]
-    sets = [dict(x=x, g=g, dy=dy, y=y, dx=dx, dg=dg, r=rstd, ws=ws)]
-    sets.append({k: torch.empty_like(v) for k, v in sets[0].items()})
-    houts = [dict(y=torch.empty_like(x_h).pin_memory(), dx=torch.empty_like(x_h).pin_memory(),
-                  dg=torch.empty_like(g_h).pin_memory(), r=torch.empty(M, dtype=torch.float32).pin_memory())
+    sets = [bufs, device_set()]
+    out_names = [k for k in op.outputs]
+    houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in out_names}
              for _ in range(2)]
 
     def e2e_step(k):
-        s, b, h = streams[k % 2], sets[k % 2], houts[k % 2]
+        s, b, ho = streams[k % 2], sets[k % 2], houts[k % 2]
         with torch.cuda.stream(s):
-            b["x"].view(-1).copy_(x_h, non_blocking=True)
-            b["g"].copy_(g_h, non_blocking=True)
-            b["dy"].view(-1).copy_(dy_h, non_blocking=True)
-            st = B.rmsnorm_fwd(b["x"], b["g"], b["y"], b["r"], M, N, w.eps, dt, int(w.offset), s)
-            st = st or B.rmsnorm_bwd(b["dy"], b["x"], b["g"], b["r"], b["dx"], b["dg"], M, N, dt, int(w.offset),
-                                     b["ws"], wsz, s)
+            for name in op.inputs:
+                b[name].copy_(host[name], non_blocking=True)
+            st = op.fwd(B, b, s) or op.bwd(B, b, s, wsz)
             if st:
                 raise B.RMSNormError(st, "end-to-end step")
-            h["y"].copy_(b["y"].view(-1), non_blocking=True)
-            h["r"].copy_(b["r"], non_blocking=True)
-            h["dx"].copy_(b["dx"].view(-1), non_blocking=True)
-            h["dg"].copy_(b["dg"], non_blocking=True)
+            for name in out_names:
+                ho[name].copy_(b[name].view(-1), non_blocking=True)
 
     e2e_step(0)
     e2e_step(1)
@@ -367,8 +451,8 @@ def run_ours(args, w):
     e1.record(streams[0])
     torch.cuda.synchronize()
     e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
-    h2d = (x_h.numel() + g_h.numel() + dy_h.numel()) * w.elem_bytes
-    d2h = (x_h.numel() * 2 + g_h.numel()) * w.elem_bytes + 4 * M
+    h2d = sum(host[k].numel() * host[k].element_size() for k in op.inputs)
+    d2h = sum(bufs[k].numel() * bufs[k].element_size() for k in out_names)
 
     if rank != 0:
         return 0
@@ -377,19 +461,20 @@ def run_ours(args, w):
     fwd_avg_ms = statistics.mean(fwd_ms)
     bwd_gbs = w.bwd_bytes() / (bwd_avg_ms / 1e3) / 1e9
     fwd_gbs = w.fwd_bytes() / (fwd_avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic(f"rmsnorm_bwd {w.name}")
+    traffic = recorded_traffic(f"{op.name}_bwd {w.name}")
+    p_fwd, p_bwd = op.passes
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "metric": metric_for(w), "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if dt == "float32" else
         {"bfloat16": "bf16", "float16": "f16"}[dt],
         "data": "synthetic (seeded; see rmsnorm_fwd_bwd_gb300/inputs.py)",
         "config": workload_config(w),
         "fwd": {"us": fwd_avg_ms * 1e3, "gbs": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
-                "bytes": w.fwd_bytes(), "plan": B.rmsnorm_describe_plan(0, M, N, dt)},
+                "bytes": w.fwd_bytes(), "plan": B.rmsnorm_describe_plan(p_fwd, M, N, dt)},
         "bwd": {"us": bwd_avg_ms * 1e3, "gbs": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
-                "bytes": w.bwd_bytes(), "plan": B.rmsnorm_describe_plan(1, M, N, dt)},
-        "roofline": {"bound": "hbm", "kernel": "rmsnorm_bwd (fused row kernel + dgamma reduce)",
+                "bytes": w.bwd_bytes(), "plan": B.rmsnorm_describe_plan(p_bwd, M, N, dt)},
+        "roofline": {"bound": "hbm", "kernel": op.kernel,
                      "achieved": bwd_gbs, "peak": peak, "peak_kind": f"{peak_kind} HBM copy",
                      "unit": "GB/s", "frac": bwd_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": w.bwd_bytes()},
@@ -400,7 +485,7 @@ def run_ours(args, w):
         "clocks": clocks.summary(0, 0),
     }
     if not args.no_cpu_baseline:
-        rate, rows, t = cpu_oracle_rate(w, x_np, g_np, dy_np, args.cpu_budget)
+        rate, rows, t = cpu_oracle_rate(w, h_np, args.cpu_budget)
         line["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": f"first {rows} rows of the workload, fwd+bwd reference, "
                                           f"{t:.1f} s"}

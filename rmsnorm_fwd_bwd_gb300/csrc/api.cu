@@ -38,19 +38,23 @@ constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per te
 //    kRingPerSm: more requests in flight lower HBM efficiency, fewer leave it
 //    latency-bound. The forward keeps 2 stages; the backward 2-4.
 constexpr int kMinVpt = 2;
-constexpr int kThreadCap[2] = {256, 128};  // forward, backward (no cluster)
+// Per pass (RMSNorm fwd, bwd, LayerNorm fwd, bwd). The LayerNorm forward reduces
+// three numbers per warp per row (four butterfly sums): fewer warps per row and
+// more rows in flight per SM hide that latency (measured: 128 threads).
+constexpr int kThreadCap[4] = {256, 128, 128, 128};  // no cluster
 // backward: elements a thread keeps in registers (x, u and dgamma sums; LayerNorm
 // also dbeta sums)
 constexpr int kMaxElemsPerThread[2] = {32, 16};  // RMSNorm, LayerNorm
-constexpr int kRingPerSm[2] = {48 << 10, 96 << 10};
+constexpr int kRingPerSm[4] = {48 << 10, 96 << 10, 64 << 10, 96 << 10};
 constexpr int kMaxBlocksPerSm = 16;
 // Rows split over a cluster pay a cluster barrier per row; there a third
-// forward stage and more resident blocks hide it better (measured).
-constexpr int kClusterThreadCap[2] = {128, 256};
-constexpr int kClusterStages[2] = {3, 2};
-constexpr int kClusterBlocksPerSm[2] = {6, 3};
-// Bound on the general path's backward workspace; more blocks than this add
-// little once every SM holds one.
+// RMSNorm forward stage and more resident blocks hide it better (measured; the
+// LayerNorm forward, with more registers per thread, is faster with two).
+constexpr int kClusterThreadCap[4] = {128, 256, 128, 256};
+constexpr int kClusterStages[4] = {3, 2, 2, 2};
+constexpr int kClusterBlocksPerSm[4] = {6, 3, 6, 3};
+// Bound on each plane of the general and row-vector paths' backward workspace;
+// more blocks than this add little once every SM holds a few.
 constexpr int64_t kScalarWorkspaceCap = int64_t(8) << 20;
 
 struct DeviceInfo {
@@ -166,7 +170,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[dir] : kThreadCap[dir]);
+        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kThreadCap[pass]);
         for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
@@ -192,31 +196,39 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     // ring shape: blocks per SM and stages aiming at kRingPerSm resident per SM
     int bps = ov.blocks_per_sm;
     int stages = ov.stages;
-    if (cl > 1) {
-        if (!stages) stages = kClusterStages[dir];
-        if (!bps) bps = kClusterBlocksPerSm[dir];
-    } else if (dir == 0) {
-        if (!stages) stages = 2;
-        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[0], 2 * stage), 2),
-                                                           kMaxBlocksPerSm));
-    } else {
-        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (2 * stage), 1), 4));
-        if (!stages)
-            stages = static_cast<int>(
-                std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (static_cast<int64_t>(bps) * stage), 2), 4));
-    }
-    while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
-    if (stages < 1) return false;
     p.path = kPathTma;
     p.dtype = dt;
     p.offset = offset;
     p.cluster = cl;
     p.threads = threads;
     p.per_thread = vpt;
-    p.stages = stages;
-    p.smem = static_cast<size_t>(stages) * (stage + 8) + fixed;
     const void* k = kernel_for(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
+    if (cl > 1) {
+        if (!stages) stages = kClusterStages[pass];
+        if (!bps) bps = kClusterBlocksPerSm[pass];
+    } else if (dir == 0) {
+        if (!stages) stages = 2;
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[pass], 2 * stage), 2),
+                                                           kMaxBlocksPerSm));
+    } else {
+        if (!bps) {
+            bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
+            // blocks that fit by registers alone: the ring depth is sized for those
+            int fit = 0;
+            p.smem = static_cast<size_t>(stage + 8) + fixed;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, threads, p.smem) == cudaSuccess && fit >= 1 &&
+                fit < bps)
+                bps = fit;
+        }
+        if (!stages)
+            stages = static_cast<int>(
+                std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (static_cast<int64_t>(bps) * stage), 2), 4));
+    }
+    while (stages > 1 && static_cast<int64_t>(stages) * (stage + 8) + fixed > di.smem_optin) --stages;
+    if (stages < 1) return false;
+    p.stages = stages;
+    p.smem = static_cast<size_t>(stages) * (stage + 8) + fixed;
     int64_t units = 0;
     if (!occupancy_units(k, p, di, bps, units)) return false;
     p.units = units < M ? units : M;
@@ -242,9 +254,8 @@ bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     int64_t units = 0;
     if (!occupancy_units(k, p, di, 0, units)) return false;
     if (planes) {
-        // keep the partials (planes x units x N floats) within kScalarWorkspaceCap
-        const int64_t cap =
-            std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(planes) * N));
+        // keep each plane of partials (units x N floats) within kScalarWorkspaceCap
+        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
         if (units > cap) units = cap;
     }
     p.units = units < M ? units : M;
@@ -271,14 +282,18 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.threads = kScalarThreads;
     p.per_thread = kv;
     p.stages = 0;
-    // gamma (and the backward's accumulators) with one padding word per 8 columns
+    // per-column fp32 arrays with one padding word per 8 columns: gamma (RMSNorm
+    // forward); gamma and dgamma sums (RMSNorm backward); gamma and beta
+    // (LayerNorm forward); gamma, dgamma and dbeta sums (LayerNorm backward)
     const size_t padded = static_cast<size_t>(N) + N / 8 + 1;
-    p.smem = padded * 4 * (pass == 0 ? 1 : 2);
-    const void* k = rowvec_kernel(pass, p);
+    const int arrays[4] = {1, 2, 2, 3};
+    p.smem = padded * 4 * arrays[pass];
+    const void* k = pass < 2 ? rowvec_kernel(pass, p) : ln_rowvec_kernel(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
     if (!occupancy_units(k, p, di, 0, units)) return false;
-    if (pass == 1) {
+    const int planes = pass == 1 ? 1 : (pass == 3 ? 2 : 0);  // workspace planes of partials
+    if (planes) {
         const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
         if (units > cap) units = cap;
     }
@@ -296,7 +311,7 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
     if (layout == kLayoutAligned && tma_shape) path = kPathTma;
-    else if (layout != kLayoutMixed && pass < 2) path = kPathRowVec;  // LayerNorm: no row-vector kernels
+    else if (layout != kLayoutMixed) path = kPathRowVec;
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
@@ -467,7 +482,8 @@ rmsnorm_status ln_fwd_impl(const void* x, int64_t ldx, const void* gamma, const 
     if (!aligned(x, s) || !aligned(gamma, s) || !aligned(beta, s) || !aligned(y, s) || !aligned(mean, 4) ||
         !aligned(rstd, 4))
         return RMSNORM_ERR_ALIGN;
-    // TMA path: 16-byte aligned rows; anything else: the general path
+    // TMA path: 16-byte aligned rows; otherwise the row-vector path (x read at
+    // each row's own phase, y written at any phase)
     const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(beta, 16) && aligned(y, 16) &&
                      (ldx * s) % 16 == 0 && (ldy * s) % 16 == 0;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -475,7 +491,7 @@ rmsnorm_status ln_fwd_impl(const void* x, int64_t ldx, const void* gamma, const 
     DeviceInfo* di = nullptr;
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(2, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
+    if (!get_plan(2, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutPhase, dev, *di, p))
         return RMSNORM_ERR_UNSUPPORTED;
     RowArgs a = {};
     a.x = x;
@@ -520,12 +536,16 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     if (!aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) || !aligned(dx, s) || !aligned(mean, 4) ||
         !aligned(rstd, 4) || !aligned(workspace, 16))
         return RMSNORM_ERR_ALIGN;
+    // as the RMSNorm backward: TMA path, row-vector path when x and dy rows
+    // share their 16-byte phase, general path otherwise
     const bool a16 = aligned(dy, 16) && aligned(x, 16) && aligned(gamma, 16) && aligned(dx, 16) &&
                      (ldx * s) % 16 == 0 && (lddy * s) % 16 == 0 && (lddx * s) % 16 == 0;
+    const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15) &&
+                            (ldx * s) % 16 == (lddy * s) % 16;
+    const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(3, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
-        return RMSNORM_ERR_UNSUPPORTED;
+    if (!get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
     const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -608,7 +628,7 @@ extern "C" size_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dty
     if (current_device(dev, di) != RMSNORM_OK) return 0;
     int64_t units = 0;
     Plan p;
-    for (int layout : {kLayoutMixed, kLayoutAligned})
+    for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
         if (get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p) && p.units > units) units = p.units;
     return 2 * static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
 }

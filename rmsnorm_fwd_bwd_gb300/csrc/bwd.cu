@@ -21,8 +21,14 @@
 
 namespace rmsnorm {
 
+// Minimum resident blocks passed to __launch_bounds__ (0: none). Left alone,
+// ptxas compiles the fp32 4-vector instance into 64 registers with spills; a
+// floor of 2 blocks (at most 128 registers) gives it 96 and no spills.
+template <int DT, int VPT> struct BwdMinBlocks { static constexpr int value = 0; };
+template <> struct BwdMinBlocks<kF32, 4> { static constexpr int value = 2; };
+
 template <int DT, int VPT, bool OFFSET, bool CLUSTER>
-__global__ void __launch_bounds__(kTmaMaxThreads) bwd_tma_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kTmaMaxThreads, (BwdMinBlocks<DT, VPT>::value)) bwd_tma_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char smem[];

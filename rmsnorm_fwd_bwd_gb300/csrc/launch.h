@@ -59,6 +59,7 @@ const void* bwd_kernel(const Plan& p);
 const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backward
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
+const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);

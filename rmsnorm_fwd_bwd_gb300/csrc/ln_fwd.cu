@@ -10,59 +10,26 @@
 //
 // Two kernels, on the same machinery as the RMSNorm forward:
 //  * ln_fwd_tma_kernel: persistent, TMA bulk-copy ring, rows split over a
-//    thread-block cluster when they are wide. The mean and the variance come
-//    from ONE reduction per row: each thread forms (count, mean, sum of squared
-//    deviations) of its own elements from registers, and these triples are
-//    merged pairwise (Chan, Golub and LeVeque's update for combining two
-//    partial variances) warp -> CTA -> cluster. The merge order is a fixed
-//    binary tree in which the lower lane's partial is always the left operand,
-//    so every thread of every CTA of the row obtains the same bits. No
+//    thread-block cluster when they are wide. The mean and the variance take
+//    ONE barrier per row. Each warp forms, from registers, the mean of its
+//    elements (a butterfly sum) and then the sum of squared deviations about
+//    that mean (a second butterfly sum): a two-pass variance within the warp.
+//    The per-warp triples (count n_w, mean m_w, deviations q_w) of the CTA, or
+//    of every CTA of the cluster through distributed shared memory, are then
+//    combined by the parallel-axis identity
+//        mu = sum_w n_w m_w / N,   q = sum_w (q_w + n_w (m_w - mu)^2)
+//    with two more butterfly sums, whose every term is non-negative. No
 //    one-pass sum-of-squares formula: rows with a large mean keep their
-//    accuracy.
-//  * ln_fwd_scalar_kernel: any N and element alignment, one CTA per row, three
+//    accuracy. Butterfly sums leave the same bits in every lane, so every
+//    thread of every CTA of the row uses the same mu and r.
+//  * ln_fwd_scalar_kernel: any N and element alignment (rows too wide for the
+//    row-vector kernels of ln_rowvec.cu), one CTA per row, three
 //    passes over the row (sum; squared deviations; output), the later ones
 //    served by L1/L2.
 #include "device.cuh"
 #include "launch.h"
 
 namespace rmsnorm {
-
-namespace {
-
-// Partial statistics of a set of n values: their mean m and q = sum (v - m)^2.
-struct MeanVar {
-    float n, m, q;
-};
-
-// Merge of two disjoint sets: n = na + nb, d = mb - ma,
-// m = ma + d * nb / n, q = qa + qb + d^2 * na * nb / n.
-__device__ __forceinline__ MeanVar mv_merge(const MeanVar& a, const MeanVar& b) {
-    MeanVar r;
-    r.n = a.n + b.n;
-    const float f = r.n > 0.f ? b.n / r.n : 0.f;
-    const float d = b.m - a.m;
-    r.m = fmaf(d, f, a.m);
-    r.q = (a.q + b.q) + (d * d) * (a.n * f);
-    return r;
-}
-
-// Butterfly merge over the 32 lanes. At distance o the partners l and l ^ o
-// both compute merge(lower lane, upper lane), so after the last level every
-// lane holds the same bits.
-__device__ __forceinline__ MeanVar warp_merge(MeanVar s) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        MeanVar t;
-        t.n = __shfl_xor_sync(0xffffffffu, s.n, o);
-        t.m = __shfl_xor_sync(0xffffffffu, s.m, o);
-        t.q = __shfl_xor_sync(0xffffffffu, s.q, o);
-        s = (lane & o) ? mv_merge(t, s) : mv_merge(s, t);
-    }
-    return s;
-}
-
-}  // namespace
 
 template <int DT, int VPT, bool CLUSTER>
 __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArgs a) {
@@ -119,11 +86,12 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
             E::unpack(idx < nvec ? __ldg(bs + idx) : make_uint4(0, 0, 0, 0), bf[v]);
         }
     }
-    // elements this thread owns in every row
+    // elements this warp owns in every row (a multiple of VEC), and its reciprocal
     int mine = 0;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) mine += (v * nt + tid < nvec) ? VEC : 0;
-    const float n_mine = static_cast<float>(mine);
+    const float n_warp = warp_allsum(static_cast<float>(mine));
+    const float inv_n_warp = n_warp > 0.f ? 1.0f / n_warp : 0.f;
 
     __syncthreads();
     if (CLUSTER) cluster_sync();  // peers' shared memory is live before any DSMEM read
@@ -149,7 +117,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
 
         if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        // x slice widened to fp32 once; this thread's mean, then its squared deviations
+        // x slice widened to fp32 once; the warp's mean, then its squared deviations
         float xf[VPT][VEC];
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -163,28 +131,25 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
                 s1 += xf[v][e + 1];
             }
         }
-        MeanVar mv;
-        mv.n = n_mine;
-        mv.m = mine ? (s0 + s1) / n_mine : 0.f;
+        const float m_warp = warp_allsum(s0 + s1) * inv_n_warp;
         float q0 = 0.f, q1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             if (v * nt + tid < nvec) {
 #pragma unroll
                 for (int e = 0; e < VEC; e += 2) {
-                    const float d0 = xf[v][e] - mv.m, d1 = xf[v][e + 1] - mv.m;
+                    const float d0 = xf[v][e] - m_warp, d1 = xf[v][e + 1] - m_warp;
                     q0 = fmaf(d0, d0, q0);
                     q1 = fmaf(d1, d1, q1);
                 }
             }
         }
-        mv.q = q0 + q1;
-        mv = warp_merge(mv);
+        const float q_warp = warp_allsum(q0 + q1);
         const int b = static_cast<int>(j & 1) * 32;
         if (lane == 0) {
-            red_n[b + warp] = mv.n;
-            red_m[b + warp] = mv.m;
-            red_q[b + warp] = mv.q;
+            red_n[b + warp] = n_warp;
+            red_m[b + warp] = m_warp;
+            red_q[b + warp] = q_warp;
         }
         // every thread has its slice in registers after this barrier: the stage can refill
         if (CLUSTER) cluster_sync(); else __syncthreads();
@@ -204,24 +169,25 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
             parity ^= 1u;
         }
 
-        // lane l holds warp (l mod nwarps) of CTA (l / nwarps); empty lanes merge as n = 0
-        MeanVar t = {0.f, 0.f, 0.f};
+        // lane l holds warp (l mod nwarps) of CTA (l / nwarps); empty lanes hold n = 0
+        float tn = 0.f, tm = 0.f, tq = 0.f;
         if (!CLUSTER) {
             if (lane < nwarps) {
-                t.n = red_n[b + lane];
-                t.m = red_m[b + lane];
-                t.q = red_q[b + lane];
+                tn = red_n[b + lane];
+                tm = red_m[b + lane];
+                tq = red_q[b + lane];
             }
         } else if (lane < nwarps * static_cast<int>(csize)) {
             const uint32_t rk = static_cast<uint32_t>(lane / nwarps);
             const int w = lane % nwarps;
-            t.n = dsmem_ld_f32(dsmem_map(smem_u32(red_n + b + w), rk));
-            t.m = dsmem_ld_f32(dsmem_map(smem_u32(red_m + b + w), rk));
-            t.q = dsmem_ld_f32(dsmem_map(smem_u32(red_q + b + w), rk));
+            tn = dsmem_ld_f32(dsmem_map(smem_u32(red_n + b + w), rk));
+            tm = dsmem_ld_f32(dsmem_map(smem_u32(red_m + b + w), rk));
+            tq = dsmem_ld_f32(dsmem_map(smem_u32(red_q + b + w), rk));
         }
-        t = warp_merge(t);
-        const float mu = t.m;
-        const float r = 1.0f / sqrtf(t.q / static_cast<float>(a.N) + a.eps);
+        const float mu = warp_allsum(tn * tm) / static_cast<float>(a.N);
+        const float dm = tm - mu;
+        const float var = warp_allsum(fmaf(tn * dm, dm, tq)) / static_cast<float>(a.N);
+        const float r = 1.0f / sqrtf(var + a.eps);
 
         if (!aborted) {
             if (tid == 0 && crank == 0) {
@@ -334,6 +300,7 @@ static const void* ln_fwd_for(const Plan& p) {
 }
 
 const void* ln_fwd_kernel(const Plan& p) {
+    if (p.path == kPathRowVec) return ln_rowvec_kernel(2, p);
     switch (p.dtype) {
     case kF32: return ln_fwd_for<kF32>(p);
     case kF16: return ln_fwd_for<kF16>(p);

@@ -18,85 +18,9 @@
 // phase are written element by element.
 #include "device.cuh"
 #include "launch.h"
+#include "rowvec.cuh"
 
 namespace rmsnorm {
-
-namespace {
-
-template <int DT> struct Raw;
-template <> struct Raw<kF32> {
-    __device__ __forceinline__ static uint32_t ld(const char* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
-};
-template <> struct Raw<kF16> {
-    __device__ __forceinline__ static uint32_t ld(const char* p) {
-        return __ldg(reinterpret_cast<const unsigned short*>(p));
-    }
-};
-template <> struct Raw<kBF16> {
-    __device__ __forceinline__ static uint32_t ld(const char* p) {
-        return __ldg(reinterpret_cast<const unsigned short*>(p));
-    }
-};
-
-// The 16-byte vector at address A (16-byte aligned) with every element outside
-// the row [rb, re) set to zero. [tb, te) is the whole tensor: a vector that
-// reaches outside it is read element by element, so no byte outside the tensor
-// is touched.
-template <int DT>
-__device__ __forceinline__ uint4 load_vec(const char* A, const char* rb, const char* re, const char* tb,
-                                          const char* te) {
-    using E = Elem<DT>;
-    if (A >= rb && A + 16 <= re) return __ldg(reinterpret_cast<const uint4*>(A));  // wholly inside the row
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (A >= tb && A + 16 <= te) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(A));
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-#pragma unroll
-        for (int e = 0; e < E::kVec; ++e) {
-            const char* p = A + e * E::kBytes;
-            if (p < rb || p >= re) {
-                if (E::kBytes == 4) w[e] = 0u;
-                else w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
-            }
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-#pragma unroll
-    for (int e = 0; e < E::kVec; ++e) {
-        const char* p = A + e * E::kBytes;
-        if (p >= rb && p < re) {
-            const uint32_t v = Raw<DT>::ld(p);
-            if (E::kBytes == 4) w[e] = v;
-            else w[e >> 1] |= v << ((e & 1) * 16);
-        }
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Load the vectors of one row that thread tid owns (tid, tid + nt, ...); the
-// row spans (ceil16(re) - floor16(rb)) / 16 vectors, the rest are zero.
-template <int DT, int KV>
-__device__ __forceinline__ void load_row(const char* base, int64_t row, size_t pitch, size_t rowb, int nt,
-                                         int tid, const char* tb, const char* te, uint4 (&v)[KV]) {
-    const char* rb = base + static_cast<size_t>(row) * pitch;
-    const char* re = rb + rowb;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(rb) & ~uintptr_t(15);
-    const int nv = static_cast<int>(((reinterpret_cast<uintptr_t>(re) + 15) & ~uintptr_t(15)) - a0) / 16;
-#pragma unroll
-    for (int k = 0; k < KV; ++k) {
-        const int idx = tid + k * nt;
-        v[k] = idx < nv ? load_vec<DT>(reinterpret_cast<const char*>(a0) + 16 * idx, rb, re, tb, te)
-                        : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// Shared-memory slot of column c. A thread owns 8 (or 4) consecutive columns, so
-// for one element position the 32 lanes of a warp touch columns 8 apart; one
-// padding word after every 8 columns puts those 32 accesses in 32 different
-// banks whatever the row's phase.
-__device__ __forceinline__ int pad_col(int c) { return c + (c >> 3); }
-
-}  // namespace
 
 template <int DT, int KV, bool OFFSET>
 __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArgs a) {
@@ -104,7 +28,7 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     extern __shared__ __align__(16) unsigned char smem[];
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma by pad_col(column)
+    float* gsm = reinterpret_cast<float*>(smem);  // gamma by rowvec::pad_col(column)
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -122,7 +46,7 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
 
     for (int c = tid; c < N; c += nt) {
         const float w = E::ld(a.gamma, c);
-        gsm[pad_col(c)] = OFFSET ? 1.0f + w : w;
+        gsm[rowvec::pad_col(c)] = OFFSET ? 1.0f + w : w;
     }
     __syncthreads();
 
@@ -130,11 +54,11 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     const int nvr = static_cast<int>(rowb / 16) + 2;
     uint4 cur[KV], nxt[KV];
     int64_t row = blockIdx.x;
-    if (row < a.M) load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cur);
+    if (row < a.M) rowvec::load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cur);
     int parity = 0;
     for (; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t next = row + gridDim.x;
-        if (next < a.M) load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nxt);
+        if (next < a.M) rowvec::load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nxt);
         const char* rb = xb + static_cast<size_t>(row) * xp;
         const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // row's byte phase
         // column of element 0 of vector idx: (16*idx - o) / S
@@ -173,7 +97,7 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
                 const int c = c0 + e;
                 const bool in = c >= 0 && c < N;
                 full = full && in;
-                const float g = in ? gsm[pad_col(c)] : 0.f;
+                const float g = in ? gsm[rowvec::pad_col(c)] : 0.f;
                 out[e] = OFFSET ? (g * f[e]) * r : (f[e] * r) * g;
             }
             if (full && same_phase) {
@@ -198,9 +122,9 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int padded = pad_col(a.N) + 1;
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma (or 1 + w) by pad_col(column)
-    float* acc = gsm + padded;                    // dgamma accumulators by pad_col(column)
+    const int padded = rowvec::pad_col(a.N) + 1;
+    float* gsm = reinterpret_cast<float*>(smem);  // gamma (or 1 + w) by rowvec::pad_col(column)
+    float* acc = gsm + padded;                    // dgamma accumulators by rowvec::pad_col(column)
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -221,8 +145,8 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
 
     for (int c = tid; c < N; c += nt) {
         const float w = E::ld(a.gamma, c);
-        gsm[pad_col(c)] = OFFSET ? 1.0f + w : w;
-        acc[pad_col(c)] = 0.f;
+        gsm[rowvec::pad_col(c)] = OFFSET ? 1.0f + w : w;
+        acc[rowvec::pad_col(c)] = 0.f;
     }
     __syncthreads();
 
@@ -230,8 +154,8 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     uint4 cx[KV], cd[KV], nx[KV], nd[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) {
-        load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cx);
-        load_row<DT, KV>(db, row, dp, rowb, nt, tid, db, de, cd);
+        rowvec::load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cx);
+        rowvec::load_row<DT, KV>(db, row, dp, rowb, nt, tid, db, de, cd);
     }
     float r_next = row < a.M ? __ldg(a.rstd_in + row) : 0.f;
     int parity = 0;
@@ -239,8 +163,8 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
         const int64_t next = row + gridDim.x;
         const float r = r_next;
         if (next < a.M) {
-            load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nx);
-            load_row<DT, KV>(db, next, dp, rowb, nt, tid, db, de, nd);
+            rowvec::load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nx);
+            rowvec::load_row<DT, KV>(db, next, dp, rowb, nt, tid, db, de, nd);
             r_next = __ldg(a.rstd_in + next);
         }
         const char* rb = xb + static_cast<size_t>(row) * xp;
@@ -258,7 +182,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
             for (int e = 0; e < VEC; ++e) {
                 const int c = c0 + e;
                 if (c >= 0 && c < N) {
-                    const int sc = pad_col(c);
+                    const int sc = rowvec::pad_col(c);
                     const float u = __fmul_rn(df[e], gsm[sc]);
                     if (e & 1) p1 = fmaf(u, xf[e], p1); else p0 = fmaf(u, xf[e], p0);
                     acc[sc] = fmaf(__fmul_rn(df[e], xf[e]), r, acc[sc]);
@@ -290,7 +214,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
                 const int c = c0 + e;
                 const bool in = c >= 0 && c < N;
                 full = full && in;
-                const float u = __fmul_rn(df[e], in ? gsm[pad_col(c)] : 0.f);
+                const float u = __fmul_rn(df[e], in ? gsm[rowvec::pad_col(c)] : 0.f);
                 out[e] = fmaf(-xf[e], kk, __fmul_rn(r, u));
             }
             if (full && same_phase) {
@@ -313,7 +237,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     __syncthreads();  // the last row's accumulator updates are done
     if (blockIdx.x < a.M) {
         float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
-        for (int c = tid; c < N; c += nt) wrow[c] = acc[pad_col(c)];
+        for (int c = tid; c < N; c += nt) wrow[c] = acc[rowvec::pad_col(c)];
     }
 }
 

@@ -3,8 +3,9 @@ the CPU oracle.
 
 Every case gates y, mean, rstd, dx, dgamma and dbeta with the golden /
 reference / target gate. Shapes cover the TMA path (one CTA per row slice),
-the cluster path (rows split over 2 and 4 CTAs), the general path (ragged or
-misaligned rows), tiny and empty inputs, rows with a large mean (where a
+the cluster path (rows split over 2 and 4 CTAs), the row-vector path (ragged or
+misaligned rows), the general path (rows over 20 KB that are not 16-byte
+multiples, x and dy at different 16-byte phases), tiny and empty inputs, rows with a large mean (where a
 one-pass variance would cancel), constant rows (variance 0), strided rows, and
 the measured LayerNorm workloads at full size on sampled rows.
 """
@@ -45,9 +46,10 @@ def _gate(x, g, b, dy, dtype, eps=1e-5, misalign=False, title="", allow_limited=
     return y, mean, rstd, dx, dg, db
 
 
-def _plan(pass_, M, N, dtype, aligned=True):
+def _plan(pass_, M, N, dtype, aligned16=1):
+    """aligned16: 1 aligned, 0 x and dy at one shared 16-byte phase, 2 different phases."""
     from rmsnorm_fwd_bwd_gb300 import binding as B
-    return B.rmsnorm_describe_plan(pass_, M, N, dtype, 1 if aligned else 2)
+    return B.rmsnorm_describe_plan(pass_, M, N, dtype, aligned16)
 
 
 # (dtype, M, N, expected path prefix of the forward plan)
@@ -60,8 +62,11 @@ SHAPES = [
     ("bfloat16", 40, 16384, "tma cluster=2"),
     ("float16", 33, 12288, "tma cluster=2"),
     ("float32", 24, 16384, "tma cluster=4"),
-    ("bfloat16", 67, 4099, "scalar"),
-    ("float32", 50, 333, "scalar"),
+    ("bfloat16", 67, 4099, "rowvec"),
+    ("float32", 50, 333, "rowvec"),
+    ("float16", 31, 9999, "rowvec"),
+    ("float32", 29, 6001, "scalar"),
+    ("bfloat16", 23, 16383, "scalar"),
 ]
 
 
@@ -74,11 +79,17 @@ def test_shapes_and_paths(dtype, M, N, path):
 
 
 @pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
-def test_misaligned_pointers_take_the_general_path(dtype):
+def test_misaligned_pointers(dtype):
+    # all tensors one element off (row-vector path, outputs at the rows' phase);
+    # only the outputs off (row-vector path, element stores); x off but dy not
+    # (the backward's general path)
     M, N = 45, 2048
+    assert _plan(2, M, N, dtype, 0).startswith("rowvec") and _plan(3, M, N, dtype, 0).startswith("rowvec")
+    assert _plan(3, M, N, dtype, 2).startswith("scalar")
     x, g, b, dy = inputs.make_ln_inputs(M, N, dtype, seed=11)
     _gate(x, g, b, dy, dtype, misalign=True, title=f"layernorm {dtype} misaligned")
     _gate(x, g, b, dy, dtype, misalign={"y", "dx"}, title=f"layernorm {dtype} misaligned outputs")
+    _gate(x, g, b, dy, dtype, misalign={"x"}, title=f"layernorm {dtype} x and dy at different phases")
 
 
 @pytest.mark.parametrize("N", [1, 2, 3])
