@@ -14,6 +14,12 @@ accelerating it" (section "Connecting Autograd and actually training"): the
 forward saves x, gamma and the per-row r; the backward returns dx and dgamma and
 nothing for eps; ``CALLS`` counts passes through the adapter so a training loop
 can prove it ran the kernel path.
+
+``layer_norm(x, weight, bias, eps)`` does the same for LayerNorm through
+``binding.layernorm_fwd`` / ``binding.layernorm_bwd`` (custom ops
+``rmsnorm_gb300::ln_fwd`` / ``rmsnorm_gb300::ln_bwd``): the forward saves x,
+gamma and the per-row mean and r; the backward returns dx, dgamma and dbeta.
+``LN_CALLS`` counts its passes.
 """
 from __future__ import annotations
 
@@ -22,6 +28,7 @@ import torch
 from . import binding
 
 CALLS = {"forward": 0, "backward": 0}
+LN_CALLS = {"forward": 0, "backward": 0}
 
 
 def _rows(x: torch.Tensor):
@@ -121,3 +128,95 @@ class RMSNorm(torch.nn.Module):
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return rms_norm(x, self.weight, self.eps, self.offset)
+
+
+# --------------------------------------------------------------------------- #
+# LayerNorm
+# --------------------------------------------------------------------------- #
+@torch.library.custom_op("rmsnorm_gb300::ln_fwd", mutates_args=())
+def _ln_fwd(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor,
+            eps: float) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    x, ldx = _row_view(x)
+    M, N = _rows(x)
+    y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = binding.layernorm_fwd(x, ldx, weight.contiguous(), bias.contiguous(), y, N, mean, rstd, M, N, eps,
+                               x.dtype, torch.cuda.current_stream(x.device))
+    if st != binding.RMSNORM_OK:
+        raise binding.RMSNormError(st, "layernorm_fwd")
+    LN_CALLS["forward"] += 1
+    return y, mean, rstd
+
+
+@_ln_fwd.register_fake
+def _(x, weight, bias, eps):
+    return (x.new_empty(x.shape), x.new_empty(x.shape[:-1], dtype=torch.float32),
+            x.new_empty(x.shape[:-1], dtype=torch.float32))
+
+
+@torch.library.custom_op("rmsnorm_gb300::ln_bwd", mutates_args=())
+def _ln_bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, mean: torch.Tensor,
+            rstd: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    dy, lddy = _row_view(dy)
+    x, ldx = _row_view(x)
+    M, N = _rows(x)
+    need = binding.layernorm_bwd_workspace_size(M, N, x.dtype)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    dx = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    dw = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
+    db = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
+    st = binding.layernorm_bwd(dy, lddy, x, ldx, weight.contiguous(), mean.contiguous(), rstd.contiguous(),
+                               dx, N, dw, db, M, N, x.dtype, ws, ws.numel(), torch.cuda.current_stream(x.device))
+    if st != binding.RMSNORM_OK:
+        raise binding.RMSNormError(st, "layernorm_bwd")
+    LN_CALLS["backward"] += 1
+    return dx, dw, db
+
+
+@_ln_bwd.register_fake
+def _(dy, x, weight, mean, rstd):
+    return x.new_empty(x.shape), weight.new_empty(weight.shape), weight.new_empty(weight.shape)
+
+
+def _ln_setup_context(ctx, inputs, output):
+    x, weight, _bias, _eps = inputs
+    _, mean, rstd = output
+    ctx.save_for_backward(x, weight, mean, rstd)
+
+
+def _ln_backward(ctx, dy, dmean, drstd):
+    del dmean, drstd  # auxiliary outputs; no gradient flows through them
+    x, weight, mean, rstd = ctx.saved_tensors
+    dx, dw, db = _ln_bwd(dy, x, weight, mean, rstd)
+    return dx, dw, db, None
+
+
+_ln_fwd.register_autograd(_ln_backward, setup_context=_ln_setup_context)
+
+
+def layer_norm(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor, eps: float = 1e-5) -> torch.Tensor:
+    """y = (x - mean) * r * weight + bias over the last dimension,
+    r = 1/sqrt(biased variance + eps)."""
+    N = x.shape[-1]
+    for name, t in (("weight", weight), ("bias", bias)):
+        if t.dim() != 1 or t.shape[0] != N:
+            raise ValueError(f"{name} must be 1-D with x.shape[-1] elements")
+        if t.dtype != x.dtype:
+            raise ValueError(f"x and {name} must share a dtype")
+    y, _, _ = torch.ops.rmsnorm_gb300.ln_fwd(x, weight, bias, float(eps))
+    return y
+
+
+class LayerNorm(torch.nn.Module):
+    """Drop-in module with a learned weight (ones) and bias (zeros) of
+    ``normalized_shape`` elements."""
+
+    def __init__(self, normalized_shape: int, eps: float = 1e-5, device=None, dtype=None):
+        super().__init__()
+        self.eps = eps
+        self.weight = torch.nn.Parameter(torch.ones(normalized_shape, device=device, dtype=dtype))
+        self.bias = torch.nn.Parameter(torch.zeros(normalized_shape, device=device, dtype=dtype))
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return layer_norm(x, self.weight, self.bias, self.eps)
