@@ -122,3 +122,25 @@ def gate_ln_outputs(x, g, b, dy, dtype, eps, y=None, mean=None, rstd=None, dx=No
             out.append(gate.check(name, gold, orc.decode(ref, dtype), tgt, dtype, rel_bound=rel,
                                   condition=cond))
     return out
+
+
+def gate_bwd_bwd_outputs(ddx, ddg, dy, x, g, dtype, offset, eps, d_dy=None, d_x=None, d_gamma=None,
+                         rows=None):
+    """Gate the RMSNorm double-backward outputs: d_dy and d_x (all rows, or
+    ``rows`` only), d_gamma (over all rows). ddg may be None (zero)."""
+    out = []
+    rel = _rel_bound(dtype)
+    if d_dy is not None or d_x is not None:
+        sl = (lambda a: a) if rows is None else (lambda a: np.ascontiguousarray(a[rows]))
+        G = orc.bwd_bwd_golden(sl(ddx), ddg, sl(dy), sl(x), g, dtype, eps=eps, offset=offset)
+        R = orc.bwd_bwd_reference(sl(ddx), ddg, sl(dy), sl(x), g, dtype, eps=eps, offset=offset)
+        for name, gold, ref, tgt in (("d_dy", G[0], R[0], d_dy), ("d_x", G[1], R[1], d_x)):
+            if tgt is not None:
+                out.append(gate.check(name, gold, orc.decode(ref, dtype), orc.decode(tgt, dtype), dtype,
+                                      rel_bound=rel))
+    if d_gamma is not None:
+        G = orc.bwd_bwd_golden(ddx, ddg, dy, x, g, dtype, eps=eps, offset=offset)
+        R = orc.bwd_bwd_reference(ddx, ddg, dy, x, g, dtype, eps=eps, offset=offset)
+        out.append(gate.check("d_gamma", G[2], orc.decode(R[2], dtype), orc.decode(d_gamma, dtype), dtype,
+                              rel_bound=rel))
+    return out

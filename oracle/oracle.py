@@ -42,6 +42,10 @@ PARITY = {
                      "vanish, dbeta = column sums of dy, hand-worked 2-element row",
     "ln_fwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
     "ln_bwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
+    "bwd_bwd_golden": "pinned: central finite differences of the (pinned) golden backward "
+                      "contracted with ddx and ddgamma, for dy, x and gamma (plain and offset); "
+                      "linearity in (ddx, ddgamma); zero cotangents give zero",
+    "bwd_bwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
 }
 
 _lock = threading.Lock()
@@ -85,6 +89,8 @@ def _load():
             "oracle_ln_bwd_golden": [P, P, P, I64, I64, D, I, P, P, P],
             "oracle_ln_fwd_reference": [P, P, P, I64, I64, F, I, P, P, P],
             "oracle_ln_bwd_reference": [P, P, P, I64, I64, F, I, P, P, P],
+            "oracle_bwd_bwd_golden": [P, P, P, P, P, I64, I64, D, I, I, P, P, P],
+            "oracle_bwd_bwd_reference": [P, P, P, P, P, I64, I64, F, I, I, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -247,3 +253,41 @@ def ln_bwd_reference(dy, x, gamma, dtype, eps=1e-5, want_dx=True):
     _load().oracle_ln_bwd_reference(_ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
                                     DTYPES[dtype], _ptr(dx), _ptr(dg), _ptr(db))
     return dx, dg, db
+
+
+# --------------------------------------------------------------------------- #
+# RMSNorm double backward
+# --------------------------------------------------------------------------- #
+def bwd_bwd_golden(ddx, ddg, dy, x, gamma, dtype, eps=1e-6, offset=False):
+    """Gradients of sum(ddx*dx) + sum(ddg*dgamma) for dy, x and gamma, fp64.
+    ddg may be None (zero). Returns ``(d_dy [M,N], d_x [M,N], d_gamma [N])``."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    dy = _check(dy, dtype, (M, N))
+    ddx = _check(ddx, dtype, (M, N))
+    gamma = _check(gamma, dtype, (N,))
+    if ddg is not None:
+        ddg = _check(ddg, dtype, (N,))
+    d_dy = np.empty((M, N), np.float64)
+    d_x = np.empty((M, N), np.float64)
+    d_g = np.empty(N, np.float64)
+    _load().oracle_bwd_bwd_golden(_ptr(ddx), _ptr(ddg), _ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
+                                  DTYPES[dtype], int(bool(offset)), _ptr(d_dy), _ptr(d_x), _ptr(d_g))
+    return d_dy, d_x, d_g
+
+
+def bwd_bwd_reference(ddx, ddg, dy, x, gamma, dtype, eps=1e-6, offset=False):
+    """Same in dtype storage with fp32 intermediates."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    dy = _check(dy, dtype, (M, N))
+    ddx = _check(ddx, dtype, (M, N))
+    gamma = _check(gamma, dtype, (N,))
+    if ddg is not None:
+        ddg = _check(ddg, dtype, (N,))
+    d_dy = np.empty((M, N), STORAGE[dtype])
+    d_x = np.empty((M, N), STORAGE[dtype])
+    d_g = np.empty(N, STORAGE[dtype])
+    _load().oracle_bwd_bwd_reference(_ptr(ddx), _ptr(ddg), _ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
+                                     DTYPES[dtype], int(bool(offset)), _ptr(d_dy), _ptr(d_x), _ptr(d_g))
+    return d_dy, d_x, d_g

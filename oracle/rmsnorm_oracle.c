@@ -491,3 +491,137 @@ void oracle_ln_bwd_reference(const void* dy, const void* x, const void* gamma, i
     free(ag);
     free(ab);
 }
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm double backward (page "Check an AI model calculation before        */
+/* accelerating it", section "Adapting the kernel and moving to production",  */
+/* which lists double backward among the extensions not yet validated). The   */
+/* backward maps (dy, x, g) to (dx, dgamma); its own gradient, for cotangents */
+/* ddx [M x N] of dx and ddg [N] of dgamma, is obtained by differentiating    */
+/* the backward formula (r depends on x: dr/dx_j = -r^3 x_j / N):             */
+/*     u = dy*g, c = mean(u*x), A = mean(ddx*x), B = mean(ddx*u),             */
+/*     D = mean(ddg*dy*x)                                  (per row)          */
+/*     d_dy = g*r*(ddx - r^2*x*A) + r*x*ddg                                   */
+/*     d_x  = r*ddg*dy - r^3*(c*ddx + u*A + x*(B + D)) + 3*r^5*c*A*x          */
+/*     d_g  = sum over rows of r*dy*(ddx - r^2*x*A)                           */
+/* g = gamma, or 1 + w with offset (then d_w = d_g). ddg may be NULL (zero).   */
+/* ------------------------------------------------------------------------- */
+
+/* d_dy[M*N], d_x[M*N], d_gamma[N] in fp64 (each may be NULL). */
+void oracle_bwd_bwd_golden(const void* ddx, const void* ddg, const void* dy, const void* x, const void* gamma,
+                           int64_t M, int64_t N, double eps, int dt, int offset, double* d_dy, double* d_x,
+                           double* d_gamma) {
+    if (d_gamma)
+        for (int64_t j = 0; j < N; ++j) d_gamma[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double xv = load_elem(x, row + j, dt);
+            ss += xv * xv;
+        }
+        const double r = 1.0 / sqrt(ss / (double)N + eps);
+        double sc = 0.0, sa = 0.0, sb = 0.0, sd = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double w = load_elem(gamma, j, dt);
+            const double g = offset ? 1.0 + w : w;
+            const double xv = load_elem(x, row + j, dt);
+            const double dyv = load_elem(dy, row + j, dt);
+            const double u = dyv * g;
+            const double t = load_elem(ddx, row + j, dt);
+            const double q = ddg ? load_elem(ddg, j, dt) : 0.0;
+            sc += u * xv;
+            sa += t * xv;
+            sb += t * u;
+            sd += q * dyv * xv;
+        }
+        const double c = sc / (double)N, A = sa / (double)N, Bm = sb / (double)N, D = sd / (double)N;
+        const double r2 = r * r, r3 = r2 * r, r5 = r3 * r2;
+        for (int64_t j = 0; j < N; ++j) {
+            const double w = load_elem(gamma, j, dt);
+            const double g = offset ? 1.0 + w : w;
+            const double xv = load_elem(x, row + j, dt);
+            const double dyv = load_elem(dy, row + j, dt);
+            const double u = dyv * g;
+            const double t = load_elem(ddx, row + j, dt);
+            const double q = ddg ? load_elem(ddg, j, dt) : 0.0;
+            const double e = t - r2 * xv * A;
+            if (d_dy) d_dy[row + j] = g * r * e + r * xv * q;
+            if (d_x) d_x[row + j] = r * q * dyv - r3 * (c * t + u * A + xv * (Bm + D)) + 3.0 * r5 * c * A * xv;
+            if (d_gamma) d_gamma[j] += r * dyv * e;
+        }
+    }
+}
+
+/* Same outputs in dtype dt from fp32 intermediates: r recomputed as in the
+ * forward reference, the four row sums sequential, then, step by step,
+ *   e = t - (r2*x)*A;  d_dy = (g*r)*e + (r*x)*q;
+ *   d_x = ((r*q)*dy - r3*((c*t + u*A) + x*(B + D))) + ((3*r5)*(c*A))*x;
+ *   d_gamma accumulates (r*dy)*e over rows in row order. */
+void oracle_bwd_bwd_reference(const void* ddx, const void* ddg, const void* dy, const void* x, const void* gamma,
+                              int64_t M, int64_t N, float eps, int dt, int offset, void* d_dy, void* d_x,
+                              void* d_gamma) {
+    float* acc = (float*)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    for (int64_t j = 0; j < N; ++j) acc[j] = 0.0f;
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * N;
+        const float r = row_rstd_f32(x, row, N, eps, dt);
+        float sc = 0.0f, sa = 0.0f, sb = 0.0f, sd = 0.0f;
+        for (int64_t j = 0; j < N; ++j) {
+            const float w = ld32(gamma, j, dt);
+            const float g = offset ? 1.0f + w : w;
+            const float xv = ld32(x, row + j, dt);
+            const float dyv = ld32(dy, row + j, dt);
+            const float u = dyv * g;
+            const float t = ld32(ddx, row + j, dt);
+            const float q = ddg ? ld32(ddg, j, dt) : 0.0f;
+            const float ux = u * xv;
+            const float tx = t * xv;
+            const float tu = t * u;
+            const float qd = q * dyv;
+            const float qdx = qd * xv;
+            sc = sc + ux;
+            sa = sa + tx;
+            sb = sb + tu;
+            sd = sd + qdx;
+        }
+        const float c = sc / (float)N, A = sa / (float)N, Bm = sb / (float)N, D = sd / (float)N;
+        const float r2 = r * r;
+        const float r3 = r2 * r;
+        const float r5 = r3 * r2;
+        const float k5 = (3.0f * r5) * (c * A);
+        const float bd = Bm + D;
+        for (int64_t j = 0; j < N; ++j) {
+            const float w = ld32(gamma, j, dt);
+            const float g = offset ? 1.0f + w : w;
+            const float xv = ld32(x, row + j, dt);
+            const float dyv = ld32(dy, row + j, dt);
+            const float u = dyv * g;
+            const float t = ld32(ddx, row + j, dt);
+            const float q = ddg ? ld32(ddg, j, dt) : 0.0f;
+            const float r2x = r2 * xv;
+            const float r2xa = r2x * A;
+            const float e = t - r2xa;
+            if (d_dy) {
+                const float a1 = (g * r) * e;
+                const float a2 = (r * xv) * q;
+                store_elem(d_dy, row + j, dt, (double)(a1 + a2));
+            }
+            if (d_x) {
+                const float b1 = (r * q) * dyv;
+                const float ct = c * t;
+                const float ua = u * A;
+                const float xbd = xv * bd;
+                const float inner = (ct + ua) + xbd;
+                const float b2 = r3 * inner;
+                const float b3 = k5 * xv;
+                store_elem(d_x, row + j, dt, (double)((b1 - b2) + b3));
+            }
+            const float re = (r * dyv) * e;
+            acc[j] = acc[j] + re;
+        }
+    }
+    if (d_gamma)
+        for (int64_t j = 0; j < N; ++j) store_elem(d_gamma, j, dt, (double)acc[j]);
+    free(acc);
+}
