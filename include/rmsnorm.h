@@ -188,8 +188,9 @@ rmsnorm_status rmsnorm_selftest_wait_timeout(uint32_t polls, rmsnorm_stream_t st
 /*
  * Launch plan the library would use, as text (for logs and tests), e.g.
  * "tma cluster=1 threads=256 vpt=2 stages=2 units=456 ...". pass: 0 = forward,
- * 1 = backward; 2 and 3: the LayerNorm forward and backward of layernorm.h (for
- * them, any aligned16 other than 1 means the general path). aligned16: 1 if the data pointers will be 16-byte aligned, 0 if
+ * 1 = backward; 2 and 3: the LayerNorm forward and backward of layernorm.h; 4:
+ * the double backward of rmsnorm_double_backward.h (for 4, any aligned16 other
+ * than 1 means the general path). aligned16: 1 if the data pointers will be 16-byte aligned, 0 if
  * not (x and dy sharing their offset from a 16-byte boundary), 2 if x and dy
  * sit at different offsets.
  * Writes at most buf_len bytes including the terminating NUL. Host-only.
@@ -199,7 +200,7 @@ rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dty
 
 /*
  * Tuning hook: override the TMA-path launch shape for one pass (0 = forward,
- * 1 = backward, 2 / 3 = LayerNorm forward / backward). threads: threads per block (multiple of 32); vpt: 16-byte
+ * 1 = backward, 2 / 3 = LayerNorm forward / backward, 4 = double backward). threads: threads per block (multiple of 32); vpt: 16-byte
  * vectors per thread (1, 2, 4 or 8); stages: pipeline depth; blocks_per_sm:
  * cap on resident blocks per SM. Any value 0 keeps the built-in choice;
  * all zeros restores the defaults. A shape that cannot hold the row makes the

@@ -20,6 +20,12 @@ can prove it ran the kernel path.
 ``rmsnorm_gb300::ln_fwd`` / ``rmsnorm_gb300::ln_bwd``): the forward saves x,
 gamma and the per-row mean and r; the backward returns dx, dgamma and dbeta.
 ``LN_CALLS`` counts its passes.
+
+The backward op has an autograd formula of its own (double backward): the
+gradients of sum(ddx * dx) + sum(ddw * dw) for dy, x and the weight come from
+``binding.rmsnorm_bwd_bwd`` (custom op ``rmsnorm_gb300::bwd_bwd``), so
+``torch.autograd.grad(..., create_graph=True)`` through ``rms_norm`` runs on the
+library's kernels at both orders. ``CALLS["double_backward"]`` counts them.
 """
 from __future__ import annotations
 
@@ -27,7 +33,7 @@ import torch
 
 from . import binding
 
-CALLS = {"forward": 0, "backward": 0}
+CALLS = {"forward": 0, "backward": 0, "double_backward": 0}
 LN_CALLS = {"forward": 0, "backward": 0}
 
 
@@ -102,6 +108,52 @@ def _backward(ctx, dy, drstd):
 
 
 _fwd.register_autograd(_backward, setup_context=_setup_context)
+
+
+@torch.library.custom_op("rmsnorm_gb300::bwd_bwd", mutates_args=())
+def _bwd_bwd(ddx: torch.Tensor, ddw: torch.Tensor, dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor,
+             rstd: torch.Tensor, offset: bool) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    ddx, ldt = _row_view(ddx)
+    dy, lddy = _row_view(dy)
+    x, ldx = _row_view(x)
+    M, N = _rows(x)
+    need = binding.rmsnorm_bwd_bwd_workspace_size(M, N, x.dtype)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    d_dy = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    d_x = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    d_w = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
+    st = binding.rmsnorm_bwd_bwd(ddx, ldt, ddw.contiguous(), dy, lddy, x, ldx, weight.contiguous(),
+                                 rstd.contiguous(), d_dy, N, d_x, N, d_w, M, N, x.dtype, int(offset), ws,
+                                 ws.numel(), torch.cuda.current_stream(x.device))
+    if st != binding.RMSNORM_OK:
+        raise binding.RMSNormError(st, "rmsnorm_bwd_bwd")
+    CALLS["double_backward"] += 1
+    return d_dy, d_x, d_w
+
+
+@_bwd_bwd.register_fake
+def _(ddx, ddw, dy, x, weight, rstd, offset):
+    return x.new_empty(x.shape), x.new_empty(x.shape), weight.new_empty(weight.shape)
+
+
+def _bwd_setup_context(ctx, inputs, output):
+    dy, x, weight, rstd, offset = inputs
+    ctx.save_for_backward(dy, x, weight, rstd)
+    ctx.offset = offset
+
+
+def _bwd_backward(ctx, ddx, ddw):
+    dy, x, weight, rstd = ctx.saved_tensors
+    if ddx is None:
+        ddx = torch.zeros_like(x)
+    if ddw is None:
+        ddw = torch.zeros_like(weight)
+    d_dy, d_x, d_w = _bwd_bwd(ddx, ddw, dy, x, weight, rstd, ctx.offset)
+    # rstd is a function of x; its dependence is already inside d_x
+    return d_dy, d_x, d_w, None, None
+
+
+_bwd.register_autograd(_bwd_backward, setup_context=_bwd_setup_context)
 
 
 def rms_norm(x: torch.Tensor, weight: torch.Tensor, eps: float = 1e-6, offset: bool = False) -> torch.Tensor:

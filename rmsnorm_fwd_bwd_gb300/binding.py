@@ -1,5 +1,5 @@
-"""Python front end of ``librmsnorm.so`` (the C ABI in ``include/rmsnorm.h`` and
-``include/layernorm.h``).
+"""Python front end of ``librmsnorm.so`` (the C ABI in ``include/rmsnorm.h``,
+``include/layernorm.h`` and ``include/rmsnorm_double_backward.h``).
 
 The functions named like the C entry points take the same arguments in the same
 order and only marshal them: a pointer argument may be a torch tensor (its
@@ -72,6 +72,9 @@ def _load():
             "layernorm_fwd": (I, [P, I64, P, P, P, I64, P, P, I64, I64, F, I, P]),
             "layernorm_bwd_workspace_size": (SZ, [I64, I64, I]),
             "layernorm_bwd": (I, [P, I64, P, I64, P, P, P, P, I64, P, P, I64, I64, I, P, SZ, P]),
+            "rmsnorm_bwd_bwd_workspace_size": (SZ, [I64, I64, I]),
+            "rmsnorm_bwd_bwd": (I, [P, I64, P, P, I64, P, I64, P, P, P, I64, P, I64, P, I64, I64, I, I, P, SZ,
+                                    P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -179,6 +182,18 @@ def layernorm_bwd(dy, lddy, x, ldx, gamma, mean, rstd, dx, lddx, dgamma, dbeta, 
                                  _addr(rstd), _addr(dx), int(lddx), _addr(dgamma), _addr(dbeta), int(M),
                                  int(N), _dtype_code(dtype), _addr(workspace), int(workspace_bytes),
                                  _stream(stream))
+
+
+def rmsnorm_bwd_bwd_workspace_size(M, N, dtype) -> int:
+    return int(_load().rmsnorm_bwd_bwd_workspace_size(int(M), int(N), _dtype_code(dtype)))
+
+
+def rmsnorm_bwd_bwd(ddx, ldddx, ddgamma, dy, lddy, x, ldx, gamma, rstd, d_dy, ldd_dy, d_x, ldd_x, d_gamma, M, N,
+                    dtype, offset, workspace, workspace_bytes, stream=None) -> int:
+    return _load().rmsnorm_bwd_bwd(_addr(ddx), int(ldddx), _addr(ddgamma), _addr(dy), int(lddy), _addr(x),
+                                   int(ldx), _addr(gamma), _addr(rstd), _addr(d_dy), int(ldd_dy), _addr(d_x),
+                                   int(ldd_x), _addr(d_gamma), int(M), int(N), _dtype_code(dtype), int(offset),
+                                   _addr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def rmsnorm_status_string(status: int) -> str:

@@ -4,7 +4,8 @@
 // kernel launches.
 //
 // Passes: 0 RMSNorm forward, 1 RMSNorm backward, 2 LayerNorm forward,
-// 3 LayerNorm backward. Odd passes are backward passes (two input streams).
+// 3 LayerNorm backward, 4 RMSNorm double backward. Passes 1, 3 and 4 are
+// backward passes (two or three input row streams, per-column accumulators).
 //
 // Argument contract (page "Check an AI model calculation before accelerating
 // it", section "The memory contract is part of the computation"): inputs are
@@ -21,6 +22,7 @@
 
 #include "../../include/layernorm.h"
 #include "../../include/rmsnorm.h"
+#include "../../include/rmsnorm_double_backward.h"
 #include "launch.h"
 
 namespace rmsnorm {
@@ -38,21 +40,28 @@ constexpr int kSliceMaxBytes = 16384;  // widest row slice one CTA stages per te
 //    kRingPerSm: more requests in flight lower HBM efficiency, fewer leave it
 //    latency-bound. The forward keeps 2 stages; the backward 2-4.
 constexpr int kMinVpt = 2;
-// Per pass (RMSNorm fwd, bwd, LayerNorm fwd, bwd). The LayerNorm forward reduces
-// three numbers per warp per row (four butterfly sums): fewer warps per row and
-// more rows in flight per SM hide that latency (measured: 128 threads).
-constexpr int kThreadCap[4] = {256, 128, 128, 128};  // no cluster
-// backward: elements a thread keeps in registers (x, u and dgamma sums; LayerNorm
-// also dbeta sums)
-constexpr int kMaxElemsPerThread[2] = {32, 16};  // RMSNorm, LayerNorm
-constexpr int kRingPerSm[4] = {48 << 10, 96 << 10, 64 << 10, 96 << 10};
+// Per pass (RMSNorm fwd, bwd, LayerNorm fwd, bwd, RMSNorm double backward). The
+// LayerNorm forward reduces three numbers per warp per row (four butterfly sums):
+// fewer warps per row and more rows in flight per SM hide that latency
+// (measured: 128 threads).
+constexpr int kPasses = 5;
+constexpr int kThreadCap[kPasses] = {256, 128, 128, 128, 128};  // no cluster
+// Row streams read per stage, reduced numbers per row, fp32 per-column planes
+// staged in shared memory (gamma; the double backward's ddgamma).
+constexpr int kInputs[kPasses] = {1, 2, 1, 2, 3};
+constexpr int kPartials[kPasses] = {1, 1, 3, 2, 4};
+constexpr int kColumnPlanes[kPasses] = {0, 1, 0, 1, 2};
+// backward passes: elements a thread keeps in registers per row (x, u and the
+// dgamma sums; LayerNorm also dbeta sums; the double backward x, dy and ddx)
+constexpr int kMaxElemsPerThread[kPasses] = {0, 32, 0, 16, 16};
+constexpr int kRingPerSm[kPasses] = {48 << 10, 96 << 10, 64 << 10, 96 << 10, 96 << 10};
 constexpr int kMaxBlocksPerSm = 16;
 // Rows split over a cluster pay a cluster barrier per row; there a third
 // RMSNorm forward stage and more resident blocks hide it better (measured; the
 // LayerNorm forward, with more registers per thread, is faster with two).
-constexpr int kClusterThreadCap[4] = {128, 256, 128, 256};
-constexpr int kClusterStages[4] = {3, 2, 2, 2};
-constexpr int kClusterBlocksPerSm[4] = {6, 3, 6, 3};
+constexpr int kClusterThreadCap[kPasses] = {128, 256, 128, 256, 256};
+constexpr int kClusterStages[kPasses] = {3, 2, 2, 2, 2};
+constexpr int kClusterBlocksPerSm[kPasses] = {6, 3, 6, 3, 3};
 // Bound on each plane of the general and row-vector paths' backward workspace;
 // more blocks than this add little once every SM holds a few.
 constexpr int64_t kScalarWorkspaceCap = int64_t(8) << 20;
@@ -70,7 +79,6 @@ struct Override {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
-constexpr int kPasses = 4;
 Override g_override[kPasses];
 unsigned g_override_gen = 0;
 std::map<std::tuple<int, int, int64_t, int, int, int, int, unsigned>, Plan> g_plans;
@@ -86,6 +94,7 @@ const void* kernel_for(int pass, const Plan& p) {
     case 1: return bwd_kernel(p);
     case 2: return ln_fwd_kernel(p);
     case 3: return ln_bwd_kernel(p);
+    case 4: return dbwd_kernel(p);
     default: return nullptr;
     }
 }
@@ -158,13 +167,17 @@ bool occupancy_units(const void* k, const Plan& p, const DeviceInfo& di, int cap
 // TMA path: rows whose byte length is a multiple of 16, split over a cluster so
 // that one CTA stages at most kSliceMaxBytes per tensor.
 bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
-    const int dir = pass & 1;     // 0 forward, 1 backward
-    const int ln = pass >> 1;     // 0 RMSNorm, 1 LayerNorm
+    const int dir = kMaxElemsPerThread[pass] > 0 ? 1 : 0;  // 0 forward, 1 backward
     const int s = elem_bytes(dt);
     const int vec = 16 / s;
     if ((static_cast<int64_t>(N) * s) % 16 != 0) return false;
+    // the double backward also splits rows so that a CTA's slice fits its register budget
+    const int64_t max_cta_elems =
+        pass == 4 ? static_cast<int64_t>(kMaxElemsPerThread[pass]) * kTmaMaxThreads : int64_t(1) << 30;
     int cl = 1;
-    while (cl <= 4 && !((static_cast<int64_t>(N) * s) / cl <= kSliceMaxBytes && N % (cl * vec) == 0)) cl *= 2;
+    while (cl <= 4 && !((static_cast<int64_t>(N) * s) / cl <= kSliceMaxBytes && N % (cl * vec) == 0 &&
+                        N / cl <= max_cta_elems))
+        cl *= 2;
     if (cl > 4) return false;
     const int nvec = N / (cl * vec);
     const Override& ov = g_override[pass];
@@ -174,8 +187,8 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
         for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         if (vpt > 8) return false;
-        if (dir == 1 && cl == 1)
-            while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread[ln] &&
+        if (dir == 1 && (cl == 1 || pass == 4))
+            while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread[pass] &&
                    round_up(ceil_div(nvec, vpt / 2), 32) <= kTmaMaxThreads)
                 vpt /= 2;  // more threads rather than more registers
         while (vpt > 1 && ceil_div(nvec, vpt / 2) <= 32) vpt /= 2;  // tiny rows: one warp
@@ -187,12 +200,10 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
     if (cl > 8) return false;
     const int slice = (N / cl) * s;
-    const int stage = (dir == 0 ? 1 : 2) * slice;
-    // warp partials [2][k][32] floats (k = 1 RMSNorm, 3 LayerNorm forward, 2
-    // LayerNorm backward), abort flag (+ the backward's fp32 gamma slice); the
-    // mbarriers are counted per stage below
-    const int partials = pass == 2 ? 3 : (pass == 3 ? 2 : 1);
-    const int fixed = 2 * partials * 32 * 4 + 16 + (dir == 0 ? 0 : (N / cl) * 4);
+    const int stage = kInputs[pass] * slice;
+    // warp partials [2][kPartials][32] floats, abort flag, fp32 per-column planes
+    // of the CTA's slice; the mbarriers are counted per stage below
+    const int fixed = 2 * kPartials[pass] * 32 * 4 + 16 + kColumnPlanes[pass] * (N / cl) * 4;
     // ring shape: blocks per SM and stages aiming at kRingPerSm resident per SM
     int bps = ov.blocks_per_sm;
     int stages = ov.stages;
@@ -247,7 +258,7 @@ bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.per_thread = 0;
     p.stages = 0;
     // backward: fp32 column accumulators, one plane per reduced gradient
-    const int planes = pass == 1 ? 1 : (pass == 3 ? 2 : 0);
+    const int planes = (pass == 1 || pass == 4) ? 1 : (pass == 3 ? 2 : 0);
     p.smem = static_cast<size_t>(planes) * N * 4;
     const void* k = kernel_for(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
@@ -286,7 +297,7 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     // forward); gamma and dgamma sums (RMSNorm backward); gamma and beta
     // (LayerNorm forward); gamma, dgamma and dbeta sums (LayerNorm backward)
     const size_t padded = static_cast<size_t>(N) + N / 8 + 1;
-    const int arrays[4] = {1, 2, 2, 3};
+    const int arrays[kPasses] = {1, 2, 2, 3, 0};
     p.smem = padded * 4 * arrays[pass];
     const void* k = pass < 2 ? rowvec_kernel(pass, p) : ln_rowvec_kernel(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
@@ -311,7 +322,7 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
     if (layout == kLayoutAligned && tma_shape) path = kPathTma;
-    else if (layout != kLayoutMixed) path = kPathRowVec;
+    else if (layout != kLayoutMixed && pass != 4) path = kPathRowVec;  // no double-backward row-vector kernel
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
@@ -321,9 +332,9 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     bool ok = false;
     if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
     else if (path == kPathRowVec) ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);
-    if (!ok && path == kPathRowVec) {
+    if (!ok && path != kPathScalar) {
         (void)cudaGetLastError();
-        path = kPathScalar;  // rows too wide for the row-vector kernels
+        path = kPathScalar;  // rows too wide for the row-vector kernels, or no TMA shape
     }
     if (path == kPathScalar) ok = plan_scalar(pass, M, N, dt, offset, dev, di, p);
     if (!ok) {
@@ -568,6 +579,69 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     return RMSNORM_OK;
 }
 
+rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma, const void* dy, int64_t lddy,
+                            const void* x, int64_t ldx, const void* gamma, const float* rstd, void* d_dy,
+                            int64_t ldd_dy, void* d_x, int64_t ldd_x, void* d_gamma, int64_t M, int64_t N,
+                            rmsnorm_dtype dtype, int offset, void* workspace, size_t workspace_bytes,
+                            rmsnorm_stream_t stream) {
+    rmsnorm_status st = check_common(M, N, dtype, offset);
+    if (st != RMSNORM_OK) return st;
+    const size_t s = elem_bytes(dtype);
+    if (!pitch_ok(ldddx, N, M, s) || !pitch_ok(lddy, N, M, s) || !pitch_ok(ldx, N, M, s) ||
+        !pitch_ok(ldd_dy, N, M, s) || !pitch_ok(ldd_x, N, M, s))
+        return RMSNORM_ERR_SHAPE;
+    if (!d_gamma) return RMSNORM_ERR_NULL;
+    if (!aligned(d_gamma, s)) return RMSNORM_ERR_ALIGN;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (M == 0) {
+        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), d_gamma, cs) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
+    if (!ddx || !dy || !x || !gamma || !rstd || !d_dy || !d_x || !workspace) return RMSNORM_ERR_NULL;
+    if (!aligned(ddx, s) || !aligned(ddgamma, s) || !aligned(dy, s) || !aligned(x, s) || !aligned(gamma, s) ||
+        !aligned(rstd, 4) || !aligned(d_dy, s) || !aligned(d_x, s) || !aligned(workspace, 16))
+        return RMSNORM_ERR_ALIGN;
+    // TMA path: every row and per-column pointer 16-byte aligned with 16-byte
+    // pitches; anything else: the general path
+    const bool a16 = aligned(ddx, 16) && aligned(ddgamma, 16) && aligned(dy, 16) && aligned(x, 16) &&
+                     aligned(gamma, 16) && aligned(d_dy, 16) && aligned(d_x, 16) && (ldddx * s) % 16 == 0 &&
+                     (lddy * s) % 16 == 0 && (ldx * s) % 16 == 0 && (ldd_dy * s) % 16 == 0 &&
+                     (ldd_x * s) % 16 == 0;
+    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
+    Plan p;
+    if (!get_plan(4, M, static_cast<int>(N), dtype, offset, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
+        return RMSNORM_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.dy = dy;
+    a.rstd_in = rstd;
+    a.ddx = ddx;
+    a.ddg = ddgamma;
+    a.d_dy = d_dy;
+    a.dx = d_x;
+    a.ws = static_cast<float*>(workspace);
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.ldx = ldx;
+    a.lddy = lddy;
+    a.ldddx = ldddx;
+    a.ldd_dy = ldd_dy;
+    a.lddx = ldd_x;
+    a.stages = p.stages;
+    a.err = di->err;
+    if (launch_rows(kernel_for(4, p), p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, d_gamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
 }  // namespace
 }  // namespace rmsnorm
 
@@ -639,6 +713,30 @@ extern "C" rmsnorm_status layernorm_bwd(const void* dy, int64_t lddy, const void
                                         size_t workspace_bytes, rmsnorm_stream_t stream) {
     return ln_bwd_impl(dy, lddy, x, ldx, gamma, mean, rstd, dx, lddx, dgamma, dbeta, M, N, dtype, workspace,
                        workspace_bytes, stream);
+}
+
+extern "C" size_t rmsnorm_bwd_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype) {
+    if (check_common(M, N, dtype, 0) != RMSNORM_OK || M == 0) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceInfo* di = nullptr;
+    if (current_device(dev, di) != RMSNORM_OK) return 0;
+    int64_t units = 0;
+    Plan p;
+    for (int layout : {kLayoutMixed, kLayoutAligned})
+        for (int off = 0; off < 2; ++off)
+            if (get_plan(4, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
+                units = p.units;
+    return static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+}
+
+extern "C" rmsnorm_status rmsnorm_bwd_bwd(const void* ddx, int64_t ldddx, const void* ddgamma, const void* dy,
+                                          int64_t lddy, const void* x, int64_t ldx, const void* gamma,
+                                          const float* rstd, void* d_dy, int64_t ldd_dy, void* d_x, int64_t ldd_x,
+                                          void* d_gamma, int64_t M, int64_t N, rmsnorm_dtype dtype, int offset,
+                                          void* workspace, size_t workspace_bytes, rmsnorm_stream_t stream) {
+    return bwd_bwd_impl(ddx, ldddx, ddgamma, dy, lddy, x, ldx, gamma, rstd, d_dy, ldd_dy, d_x, ldd_x, d_gamma, M,
+                        N, dtype, offset, workspace, workspace_bytes, stream);
 }
 
 extern "C" const char* rmsnorm_status_string(rmsnorm_status status) {

@@ -21,6 +21,10 @@ struct RowArgs {
     const void* beta;      // LayerNorm forward
     float* mean_out;       // LayerNorm forward output (may be null, as may rstd_out there)
     const float* mean_in;  // LayerNorm backward: saved mean per row
+    const void* ddx;       // double backward: cotangent of dx [M rows, pitch ldddx]
+    const void* ddg;       // double backward: cotangent of dgamma [N] (may be null: zero)
+    void* d_dy;            // double backward output [M rows, pitch ldd_dy]; d_x goes to dx
+    int64_t ldddx, ldd_dy;
     int64_t M;
     int N;
     int64_t ldx, ldy, lddy, lddx;  // row pitches in elements (>= N)
@@ -60,6 +64,7 @@ const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backwa
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
+const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA or scalar path)
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);

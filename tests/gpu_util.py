@@ -156,3 +156,47 @@ def ln_run(x, g, b, dy, dtype, eps=1e-5, misalign=False, do_bwd=True, stats=True
         res[4] = B.to_numpy(dgt, dtype)
         res[5] = B.to_numpy(dbt, dtype)
     return tuple(res)
+
+
+def dbwd_run(ddx, ddg, dy, x, g, dtype, offset=False, eps=1e-6, misalign=False, stream=None):
+    """RMSNorm forward (for r) then the double backward through the C ABI, dense
+    rows. ddg may be None. Returns numpy storage arrays (d_dy, d_x, d_gamma).
+
+    misalign: False, True, or a set of names among {"ddx", "dy", "x", "d_dy", "d_x"}."""
+    torch = _torch()
+    M, N = x.shape
+    names = {"ddx", "dy", "x", "d_dy", "d_x"} if misalign is True else set(misalign or ())
+    keep = []
+    _, xt = _place(x, dtype, "x" in names); keep.append(_)
+    _, gt = _place(g, dtype, False); keep.append(_)
+    _, dyt = _place(dy, dtype, "dy" in names); keep.append(_)
+    _, tt = _place(ddx, dtype, "ddx" in names); keep.append(_)
+    qt = None
+    if ddg is not None:
+        _, qt = _place(ddg, dtype, False); keep.append(_)
+    rstd = torch.empty(M, dtype=torch.float32, device="cuda")
+    y = torch.empty(M * N, dtype=xt.dtype, device="cuda")
+    st = B.rmsnorm_fwd(xt, gt, y, rstd, M, N, eps, dtype, int(offset), stream)
+    assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+
+    def out(n, name):
+        buf, view = _guarded(n, dtype)
+        if name in names:
+            b2 = torch.empty(n + 2 * GUARD + 1, dtype=view.dtype, device=view.device)
+            b2[1:] = buf
+            buf, view = b2[1:], b2[1 + GUARD:1 + GUARD + n]
+        return buf, view
+
+    odybuf, ody = out(M * N, "d_dy")
+    oxbuf, ox = out(M * N, "d_x")
+    ogbuf, og = _guarded(N, dtype)
+    wsz = B.rmsnorm_bwd_bwd_workspace_size(M, N, dtype)
+    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device="cuda")
+    st = B.rmsnorm_bwd_bwd(tt, N, qt, dyt, N, xt, N, gt, rstd, ody, N, ox, N, og, M, N, dtype, int(offset),
+                           ws, wsz, stream)
+    assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
+    torch.cuda.synchronize()
+    assert _guards_intact(odybuf, dtype), "double backward wrote outside d_dy"
+    assert _guards_intact(oxbuf, dtype), "double backward wrote outside d_x"
+    assert _guards_intact(ogbuf, dtype), "double backward wrote outside d_gamma"
+    return (B.to_numpy(ody, dtype).reshape(M, N), B.to_numpy(ox, dtype).reshape(M, N), B.to_numpy(og, dtype))

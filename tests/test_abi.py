@@ -62,9 +62,10 @@ def test_host_validation_without_gpu():
     assert B.rmsnorm_bwd_workspace_size(0, 8, 0) == 0
     assert B.rmsnorm_bwd_workspace_size(4, 0, 0) == 0
     assert B.rmsnorm_bwd_workspace_size(4, 8, 9) == 0
-    assert B.rmsnorm_set_launch_override(4, 0, 0, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(5, 0, 0, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(-1, 0, 0, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(3, 0, 0, 0, 0) == 0
+    assert B.rmsnorm_set_launch_override(4, 0, 0, 0, 0) == 0
     assert B.rmsnorm_set_launch_override(0, 33, 0, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(0, 0, 3, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(0, 0, 0, 0, 0) == 0
@@ -89,6 +90,20 @@ def test_layernorm_host_validation_without_gpu():
     assert B.layernorm_bwd(None, 8, None, 9, None, None, None, None, 8, 0x1000, 0x2000, 4, 10, 0, None, 0, 0) == 2
     assert B.layernorm_bwd_workspace_size(0, 8, 0) == 0
     assert B.layernorm_bwd_workspace_size(4, 8, 9) == 0
+
+
+def test_double_backward_host_validation_without_gpu():
+    # rmsnorm_bwd_bwd(ddx, ldddx, ddg, dy, lddy, x, ldx, gamma, rstd, d_dy, ldd_dy, d_x, ldd_x, d_gamma,
+    #                 M, N, dtype, offset, ws, bytes, stream)
+    f = B.rmsnorm_bwd_bwd
+    assert f(None, 8, None, None, 8, None, 8, None, None, None, 8, None, 8, 0x1000, 4, 8, 5, 0, None, 0, 0) == 3
+    assert f(None, 8, None, None, 8, None, 8, None, None, None, 8, None, 8, 0x1000, 4, 8, 0, 2, None, 0, 0) == 9
+    assert f(None, 7, None, None, 8, None, 8, None, None, None, 8, None, 8, 0x1000, 4, 8, 0, 0, None, 0, 0) == 2
+    assert f(None, 8, None, None, 8, None, 8, None, None, None, 8, None, 8, None, 4, 8, 0, 0, None, 0, 0) == 1
+    assert f(None, 8, None, None, 8, None, 8, None, None, None, 8, None, 8, 0x1001, 4, 8, 1, 0, None, 0, 0) == 5
+    assert f(None, 8, None, None, 8, None, 8, None, None, None, 8, None, 8, 0x1000, 4, 8, 0, 0, None, 0, 0) == 1
+    assert B.rmsnorm_bwd_bwd_workspace_size(0, 8, 0) == 0
+    assert B.rmsnorm_bwd_bwd_workspace_size(4, 8, 9) == 0
 
 
 def test_library_is_in_tree_and_built_for_sm_103a():
