@@ -19,6 +19,11 @@ roofline = the backward pass (the dominant cost) against the measured HBM copy
 cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
          fp32-intermediate reference) on a bounded row sample of the workload.
 
+--double-backward: the step is one RMSNorm double backward (rmsnorm_bwd_bwd:
+         fused row kernel + d_gamma column reduction) on the workload, with
+         cotangents ddx ~ N(0,1), ddgamma ~ N(0,1); r comes from one untimed
+         forward. Algorithmic bytes = 5*M*N*s + 3*N*s + 4*M (read x, dy, ddx,
+         gamma, ddgamma, rstd; write d_dy, d_x, d_gamma).
 --workload ln_*: the same step for LayerNorm (layernorm_fwd + layernorm_bwd:
          fused row kernel + dgamma/dbeta column reduction); its algorithmic
          bytes add beta and dbeta (N*s each) and the saved mean (4*M each way).
@@ -493,6 +498,145 @@ def run_ours(args, w):
     return 0
 
 
+def run_double_backward(args, w):
+    import torch
+    from rmsnorm_fwd_bwd_gb300 import binding as B
+    from rmsnorm_fwd_bwd_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    dt, M, N, s = w.dtype, w.M, w.N, w.elem_bytes
+    x_np, g_np, dy_np = inputs.workload_inputs(w)
+    ddx_np = inputs.to_storage(inputs.normal(w.seed, 3, (M, N)), dt)
+    ddg_np = inputs.to_storage(inputs.normal(w.seed, 4, (N,)), dt)
+    host = {k: B.to_device(v.reshape(-1), dt, "cpu").pin_memory()
+            for k, v in (("x", x_np), ("g", g_np), ("dy", dy_np), ("ddx", ddx_np), ("ddg", ddg_np))}
+    wsz = B.rmsnorm_bwd_bwd_workspace_size(M, N, dt)
+
+    def device_set():
+        b = {k: v.to(dev) for k, v in host.items()}
+        b["r"] = torch.empty(M, dtype=torch.float32, device=dev)
+        b["d_dy"] = torch.empty_like(b["x"])
+        b["d_x"] = torch.empty_like(b["x"])
+        b["d_g"] = torch.empty_like(b["g"])
+        b["ws"] = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+        y = torch.empty_like(b["x"])
+        st = B.rmsnorm_fwd(b["x"], b["g"], y, b["r"], M, N, w.eps, dt, int(w.offset), stream)
+        if st:
+            raise B.RMSNormError(st, "rmsnorm_fwd")
+        return b
+
+    def step(b, strm):
+        return B.rmsnorm_bwd_bwd(b["ddx"], N, b["ddg"], b["dy"], N, b["x"], N, b["g"], b["r"], b["d_dy"], N,
+                                 b["d_x"], N, b["d_g"], M, N, dt, int(w.offset), b["ws"], wsz, strm)
+
+    bufs = device_set()
+    flush = None
+    if M * N * s < 256e6:
+        flush = torch.empty(int(512e6), dtype=torch.uint8, device=dev)
+    B.rmsnorm_device_error(clear=True)
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        st = step(bufs, stream)
+        if st:
+            raise B.RMSNormError(st, "rmsnorm_bwd_bwd")
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        step(bufs, stream)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    if flush is None:
+        total_ms = ev[0][0].elapsed_time(ev[K - 1][1])
+    else:
+        total_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    dev_err = B.rmsnorm_device_error(clear=True)
+    secs = max_over_ranks(total_ms / 1e3, world, device=dev)
+    nbytes = 5 * M * N * s + 3 * N * s + 4 * M
+    value = aggregate(nbytes, K, world, secs)
+
+    # end to end with host buffers: each step copies ddx, ddgamma, dy, x, gamma and
+    # rstd in and d_dy, d_x, d_gamma out; two streams alternate as in the main bench
+    e2e_steps = max(3, min(K, args.e2e_steps))
+    streams = [stream, torch.cuda.Stream(dev)]
+    sets = [bufs, device_set()]
+    r_host = bufs["r"].cpu().pin_memory()
+    houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in ("d_dy", "d_x", "d_g")}
+             for _ in range(2)]
+
+    def e2e_step(k):
+        strm, b, ho = streams[k % 2], sets[k % 2], houts[k % 2]
+        with torch.cuda.stream(strm):
+            for name in ("ddx", "ddg", "dy", "x", "g"):
+                b[name].copy_(host[name], non_blocking=True)
+            b["r"].copy_(r_host, non_blocking=True)
+            st = step(b, strm)
+            if st:
+                raise B.RMSNormError(st, "end-to-end double backward")
+            for name in ("d_dy", "d_x", "d_g"):
+                ho[name].copy_(b[name].view(-1), non_blocking=True)
+
+    e2e_step(0)
+    e2e_step(1)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(streams[0])
+    streams[1].wait_event(e0)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
+    torch.cuda.synchronize()
+    e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in host) + 4 * M
+    d2h = 2 * M * N * s + N * s
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    avg_ms = statistics.mean(step_ms)
+    gbs = nbytes / (avg_ms / 1e3) / 1e9
+    line = {
+        "metric": f"RMSNorm double backward HBM GB/s & % of peak, {dt} M={M} N={N}, 1 GB300",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if dt == "float32" else {"bfloat16": "bf16", "float16": "f16"}[dt],
+        "data": "synthetic (seeded; see rmsnorm_fwd_bwd_gb300/inputs.py; cotangents tags 3 and 4)",
+        "config": dict(workload_config(w), workload=f"RMSNorm double backward {dt} M={M} N={N} eps={w.eps:g}"
+                       + (" offset" if w.offset else "")),
+        "dbwd": {"us": avg_ms * 1e3, "gbs": gbs, "frac_of_peak": gbs / peak, "bytes": nbytes,
+                 "plan": B.rmsnorm_describe_plan(4, M, N, dt)},
+        "roofline": {"bound": "hbm", "kernel": "rmsnorm_bwd_bwd (fused row kernel + d_gamma reduce)",
+                     "achieved": gbs, "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": recorded_traffic(f"rmsnorm_bwd_bwd {w.name}"),
+                     "algorithmic_bytes": nbytes},
+        "e2e": {"value": nbytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 2 * K,
+        "device_error_word": dev_err,
+        "clocks": clocks.summary(0, 0),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,6 +647,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--double-backward", action="store_true",
+                    help="time the RMSNorm double backward on the workload instead of fwd+bwd")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the row count M (small cases for profiler captures)")
     args = ap.parse_args(argv)
@@ -513,6 +659,10 @@ def main(argv=None):
         w = dataclasses.replace(w, M=args.rows, name=f"{w.name}@rows={args.rows}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.double_backward:
+        if w.op != "rmsnorm":
+            ap.error("--double-backward applies to RMSNorm workloads")
+        return run_double_backward(args, w)
     return run_ours(args, w)
 
 
