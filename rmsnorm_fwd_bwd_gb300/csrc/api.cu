@@ -297,12 +297,12 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.threads = static_cast<int>(std::min<int64_t>(round_up(ceil_div(nvr, kv), 32), kScalarThreads));
     p.per_thread = kv;
     p.stages = 0;
-    // per-column fp32 arrays with one padding word per 8 columns: gamma (RMSNorm
-    // forward); gamma and dgamma sums (RMSNorm backward); gamma and beta
-    // (LayerNorm forward); gamma, dgamma and dbeta sums (LayerNorm backward)
-    const size_t padded = static_cast<size_t>(N) + N / 8 + 1;
-    const int arrays[kPasses] = {1, 2, 2, 3, 0};
-    p.smem = padded * 4 * arrays[pass];
+    // per-column fp32 data in shared memory, one VEC-float slot per 16-byte
+    // vector of the row's span: none (RMSNorm forward: gamma in registers), gamma
+    // (the backwards), gamma and beta (LayerNorm forward)
+    const int vec = 16 / elem_bytes(dt);
+    const int sets[kPasses] = {0, 1, 2, 1, 0};
+    p.smem = static_cast<size_t>(sets[pass]) * static_cast<size_t>(nvr) * vec * 4;
     const void* k = pass < 2 ? rowvec_kernel(pass, p) : ln_rowvec_kernel(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
     int64_t units = 0;
@@ -312,7 +312,11 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
         const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
         if (units > cap) units = cap;
     }
-    p.units = units < M ? units : M;
+    // a multiple of kRowVecPhases, so that every block's rows share one 16-byte
+    // phase whatever the pitch; blocks beyond the last row are idle (the
+    // backward's still write a zero row of partials)
+    units = std::max<int64_t>(kRowVecPhases, units / kRowVecPhases * kRowVecPhases);
+    p.units = std::min<int64_t>(units, round_up(M, kRowVecPhases));
     return true;
 }
 

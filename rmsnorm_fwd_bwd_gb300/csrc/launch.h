@@ -37,6 +37,10 @@ enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2 };
 
 // Most 16-byte vectors per thread on the row-vector path (256 threads).
 constexpr int kRowVecMaxKv = 5;
+// Row-vector grids are a multiple of this: rows r and r + 8 always start at the
+// same 16-byte phase (a pitch is a whole number of 2-byte elements at least), so
+// all rows of a persistent block (blockIdx.x + k * gridDim.x) share one phase.
+constexpr int kRowVecPhases = 8;
 
 // Thread caps (also the kernels' __launch_bounds__): a TMA-path slice is at most
 // 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over

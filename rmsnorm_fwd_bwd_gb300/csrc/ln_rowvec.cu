@@ -5,35 +5,47 @@
 //
 // Loads as in rowvec.cu: thread t holds vectors t, t + nt, ... of the row's
 // 16-byte aligned span in registers (elements outside the row masked to zero),
-// the next row of the block is loaded while the current one is reduced, and
-// per-column data live in shared memory at padded slots. Because a row's
-// phase decides how many of its elements each warp holds, the forward counts
-// them per row; its statistics take one barrier per row as in ln_fwd.cu: a
-// two-pass mean and squared deviations within each warp, then the
-// parallel-axis combination of the warps. The backward keeps dgamma and dbeta
-// accumulators per column in shared memory and leaves one row of each per
-// block in the workspace (two planes) for the fixed-order column reduce.
+// and the next row of the block is loaded while the current one is reduced. The
+// grid is a multiple of the 16-byte phase period, so every row of a block
+// starts at one phase and each thread owns the same columns in all of them:
+// gamma and beta are staged once per block in shared memory by vector slot, the
+// elements each warp holds are counted once, and the backward's dgamma and dbeta
+// sums stay in registers (one row of each per block in the workspace, for the
+// fixed-order column reduce). The forward's statistics take one barrier per row
+// as in ln_fwd.cu: a two-pass mean and squared deviations within each warp, then
+// the parallel-axis combination of the warps.
 #include "device.cuh"
 #include "launch.h"
 #include "rowvec.cuh"
 
 namespace rmsnorm {
 
-// Minimum resident blocks passed to __launch_bounds__ (0: none). Up to three
-// vectors per thread the forward fits 64 registers without spills, i.e. four
-// 256-thread blocks per SM; left alone ptxas uses 80-100 (two blocks).
-template <int KV> struct LnFwdRowMinBlocks { static constexpr int value = KV <= 3 ? 4 : 0; };
+// gamma and beta of the block's vector slots (VEC/4 float4 planes each, zero
+// outside the row); every row of the block starts at 16-byte phase o
+template <int DT>
+__device__ __forceinline__ void stage_columns(const void* src, int N, int o, int nvr, float4* dst) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    for (int idx = threadIdx.x; idx < nvr; idx += blockDim.x) {
+        const int c0 = (16 * idx - o) / E::kBytes;
+        float w[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int c = c0 + e;
+            w[e] = (c >= 0 && c < N) ? E::ld(src, c) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < VEC; q += 4) dst[(q / 4) * nvr + idx] = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+    }
+}
 
 template <int DT, int KV>
-__global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value))
+__global__ void __launch_bounds__(kScalarThreads, (rowvec::FwdMinBlocks<KV>::value))
     ln_fwd_rowvec_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int padded = rowvec::pad_col(a.N) + 1;
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma by padded column slot
-    float* bsm = gsm + padded;                    // beta by padded column slot
     __shared__ float red[2][3][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -47,15 +59,34 @@ __global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value)
     const char* xb = static_cast<const char*>(a.x);
     const char* xe = xb + static_cast<size_t>(a.M - 1) * xp + rowb;  // last byte of the tensor + 1
     char* yb = static_cast<char*>(a.y);
+    // every row of this block (the grid is a multiple of the phase period) starts at phase o
+    const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(blockIdx.x) * xp) & 15);
+    const int nvr = static_cast<int>(rowb / 16) + 2;  // vectors spanned by any row
+    float4* gsm4 = reinterpret_cast<float4*>(smem);
+    float4* bsm4 = gsm4 + (VEC / 4) * nvr;
     griddep_wait();
+    stage_columns<DT>(a.gamma, N, o, nvr, gsm4);
+    stage_columns<DT>(a.beta, N, o, nvr, bsm4);
 
-    for (int c = tid; c < N; c += nt) {
-        gsm[rowvec::pad_col(c)] = E::ld(a.gamma, c);
-        bsm[rowvec::pad_col(c)] = E::ld(a.beta, c);
+    // elements of a row this thread and its warp hold: the same for every row here
+    unsigned in_mask[KV];  // bit e of word k: element e of vector k is in the row
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        const int c0 = (16 * idx - o) / S;
+        in_mask[k] = 0u;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (idx < nvr && c0 + e >= 0 && c0 + e < N) {
+                in_mask[k] |= 1u << e;
+                ++cnt;
+            }
     }
+    const float n_warp = warp_allsum(static_cast<float>(cnt));
+    const float inv_n_warp = n_warp > 0.f ? 1.0f / n_warp : 0.f;
     __syncthreads();
 
-    const int nvr = static_cast<int>(rowb / 16) + 2;  // vectors spanned by any row
     uint4 cur[KV], nxt[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) rowvec::load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cur);
@@ -63,15 +94,10 @@ __global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value)
     for (; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t next = row + gridDim.x;
         if (next < a.M) rowvec::load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nxt);
-        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(row) * xp) & 15);
-
-        // elements of the row this thread holds (masked ones are zero), and their sum
+        // the warp's mean (masked elements are zero), then its squared deviations
         float s0 = 0.f, s1 = 0.f;
-        int cnt = 0;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-            const int idx = tid + k * nt;
-            const int c0 = (16 * idx - o) / S;
             float f[VEC];
             E::unpack(cur[k], f);
 #pragma unroll
@@ -79,25 +105,16 @@ __global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value)
                 s0 += f[e];
                 s1 += f[e + 1];
             }
-            if (idx < nvr) {
-                const int lo = c0 < 0 ? 0 : c0;
-                const int hi = c0 + VEC < N ? c0 + VEC : N;
-                cnt += hi > lo ? hi - lo : 0;
-            }
         }
-        const float n_warp = warp_allsum(static_cast<float>(cnt));
-        const float m_warp = n_warp > 0.f ? warp_allsum(s0 + s1) / n_warp : 0.f;
+        const float m_warp = warp_allsum(s0 + s1) * inv_n_warp;
         float q0 = 0.f, q1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-            const int idx = tid + k * nt;
-            const int c0 = (16 * idx - o) / S;
             float f[VEC];
             E::unpack(cur[k], f);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                const float d = (idx < nvr && c >= 0 && c < N) ? f[e] - m_warp : 0.f;
+                const float d = ((in_mask[k] >> e) & 1u) ? f[e] - m_warp : 0.f;
                 if (e & 1) q1 = fmaf(d, d, q1); else q0 = fmaf(d, d, q0);
             }
         }
@@ -127,26 +144,24 @@ __global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value)
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float f[VEC], out[VEC];
             E::unpack(cur[k], f);
-            bool full = true;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                const bool in = c >= 0 && c < N;
-                full = full && in;
-                const int sc = rowvec::pad_col(in ? c : 0);
-                out[e] = fmaf((f[e] - mu) * r, gsm[sc], bsm[sc]);
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 g4 = gsm4[(q / 4) * nvr + idx];
+                const float4 b4 = bsm4[(q / 4) * nvr + idx];
+                out[q] = fmaf((f[q] - mu) * r, g4.x, b4.x);
+                out[q + 1] = fmaf((f[q + 1] - mu) * r, g4.y, b4.y);
+                out[q + 2] = fmaf((f[q + 2] - mu) * r, g4.z, b4.z);
+                out[q + 3] = fmaf((f[q + 3] - mu) * r, g4.w, b4.w);
             }
-            if (full && same_phase) {
+            if (in_mask[k] == (1u << VEC) - 1u && same_phase) {
                 stg128(ya0 + 16 * idx, E::pack(out));
             } else {
+                const int c0 = (16 * idx - o) / S;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const int c = c0 + e;
-                    if (c >= 0 && c < N) E::st(yrow, c, out[e]);
-                }
+                for (int e = 0; e < VEC; ++e)
+                    if ((in_mask[k] >> e) & 1u) E::st(yrow, c0 + e, out[e]);
             }
         }
 #pragma unroll
@@ -155,25 +170,12 @@ __global__ void __launch_bounds__(kScalarThreads, (LnFwdRowMinBlocks<KV>::value)
     griddep_launch_dependents();
 }
 
-// Minimum resident blocks passed to __launch_bounds__ (0: none): left alone,
-// these instances compile into 48-64 registers with spills; the fp32 ones fit
-// 64 registers without spills when asked for four blocks.
-template <int DT, int KV> struct LnBwdRowMinBlocks { static constexpr int value = 0; };
-template <> struct LnBwdRowMinBlocks<kF32, 2> { static constexpr int value = 4; };
-template <> struct LnBwdRowMinBlocks<kF32, 3> { static constexpr int value = 4; };
-template <> struct LnBwdRowMinBlocks<kF16, 1> { static constexpr int value = 2; };
-
 template <int DT, int KV>
-__global__ void __launch_bounds__(kScalarThreads, (LnBwdRowMinBlocks<DT, KV>::value))
-    ln_bwd_rowvec_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kScalarThreads) ln_bwd_rowvec_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int padded = rowvec::pad_col(a.N) + 1;
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma by padded column slot
-    float* accg = gsm + padded;                   // dgamma accumulators
-    float* accb = accg + padded;                  // dbeta accumulators
     __shared__ float red[2][2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -190,17 +192,26 @@ __global__ void __launch_bounds__(kScalarThreads, (LnBwdRowMinBlocks<DT, KV>::va
     const char* db = static_cast<const char*>(a.dy);
     const char* de = db + static_cast<size_t>(a.M - 1) * dp + rowb;
     char* dxb = static_cast<char*>(a.dx);
+    const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(blockIdx.x) * xp) & 15);
+    const int nvr = static_cast<int>(rowb / 16) + 2;
+    float4* gsm4 = reinterpret_cast<float4*>(smem);
     griddep_wait();
-
-    for (int c = tid; c < N; c += nt) {
-        const int sc = rowvec::pad_col(c);
-        gsm[sc] = E::ld(a.gamma, c);
-        accg[sc] = 0.f;
-        accb[sc] = 0.f;
+    stage_columns<DT>(a.gamma, N, o, nvr, gsm4);
+    unsigned in_mask[KV];
+    float accg[KV][VEC], accb[KV][VEC];
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        const int c0 = (16 * idx - o) / S;
+        in_mask[k] = 0u;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            if (idx < nvr && c0 + e >= 0 && c0 + e < N) in_mask[k] |= 1u << e;
+            accg[k][e] = accb[k][e] = 0.f;
+        }
     }
     __syncthreads();
 
-    const int nvr = static_cast<int>(rowb / 16) + 2;
     uint4 cx[KV], cd[KV], nx[KV], nd[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) {
@@ -220,27 +231,27 @@ __global__ void __launch_bounds__(kScalarThreads, (LnBwdRowMinBlocks<DT, KV>::va
             m_next = __ldg(a.mean_in + next);
             r_next = __ldg(a.rstd_in + next);
         }
-        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(row) * xp) & 15);
+        // masked elements: dy = 0 and gamma = 0, so u = 0; x_hat is masked explicitly
         float p0 = 0.f, p1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float xf[VEC], df[VEC];
             E::unpack(cx[k], xf);
             E::unpack(cd[k], df);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                if (c >= 0 && c < N) {
-                    const int sc = rowvec::pad_col(c);
-                    const float xh = __fmul_rn(xf[e] - mu, r);
-                    const float u = __fmul_rn(df[e], gsm[sc]);
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 g4 = gsm4[(q / 4) * nvr + idx];
+                const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float xh = ((in_mask[k] >> (q + e)) & 1u) ? __fmul_rn(xf[q + e] - mu, r) : 0.f;
+                    const float u = __fmul_rn(df[q + e], g[e]);
                     p0 += u;
                     p1 = fmaf(u, xh, p1);
-                    accg[sc] = fmaf(df[e], xh, accg[sc]);
-                    accb[sc] += df[e];
+                    accg[k][q + e] = fmaf(df[q + e], xh, accg[k][q + e]);
+                    accb[k][q + e] += df[q + e];
                 }
             }
         }
@@ -261,28 +272,27 @@ __global__ void __launch_bounds__(kScalarThreads, (LnBwdRowMinBlocks<DT, KV>::va
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float xf[VEC], df[VEC], out[VEC];
             E::unpack(cx[k], xf);
             E::unpack(cd[k], df);
-            bool full = true;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                const bool in = c >= 0 && c < N;
-                full = full && in;
-                const float xh = __fmul_rn(xf[e] - mu, r);
-                const float u = __fmul_rn(df[e], gsm[rowvec::pad_col(in ? c : 0)]);
-                out[e] = r * fmaf(-xh, c2, u - c1);
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 g4 = gsm4[(q / 4) * nvr + idx];
+                const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float xh = __fmul_rn(xf[q + e] - mu, r);
+                    const float u = __fmul_rn(df[q + e], g[e]);
+                    out[q + e] = r * fmaf(-xh, c2, u - c1);
+                }
             }
-            if (full && same_phase) {
+            if (in_mask[k] == (1u << VEC) - 1u && same_phase) {
                 stg128(da0 + 16 * idx, E::pack(out));
             } else {
+                const int c0 = (16 * idx - o) / S;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const int c = c0 + e;
-                    if (c >= 0 && c < N) E::st(dxrow, c, out[e]);
-                }
+                for (int e = 0; e < VEC; ++e)
+                    if ((in_mask[k] >> e) & 1u) E::st(dxrow, c0 + e, out[e]);
             }
         }
 #pragma unroll
@@ -292,15 +302,21 @@ __global__ void __launch_bounds__(kScalarThreads, (LnBwdRowMinBlocks<DT, KV>::va
         }
     }
     griddep_launch_dependents();
-    __syncthreads();  // the last row's accumulator updates are done
-    if (blockIdx.x < a.M) {
-        const size_t plane = static_cast<size_t>(gridDim.x) * N;
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
-        for (int c = tid; c < N; c += nt) {
-            const int sc = rowvec::pad_col(c);
-            wrow[c] = accg[sc];
-            wrow[plane + c] = accb[sc];
-        }
+    // one row of dgamma partials (plane 0) and dbeta partials (plane 1) per block,
+    // zeros for a block without rows; the vector slots tile the row
+    const size_t plane = static_cast<size_t>(gridDim.x) * N;
+    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        if (idx >= nvr) continue;
+        const int c0 = (16 * idx - o) / S;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if ((in_mask[k] >> e) & 1u) {
+                wrow[c0 + e] = accg[k][e];
+                wrow[plane + c0 + e] = accb[k][e];
+            }
     }
 }
 

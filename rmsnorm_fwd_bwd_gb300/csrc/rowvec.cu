@@ -11,8 +11,10 @@
 // before the tensor's first byte or past its last byte is loaded element by
 // element, so every access stays inside the tensor. The next row of the block
 // is loaded into registers while the current one is reduced (one row of
-// prefetch). Gamma (or 1 + w) is staged once per block in shared memory as fp32
-// indexed by column. Outputs with the same 16-byte phase as x get 16-byte
+// prefetch). The grid is a multiple of 8, so all rows of a block start at the
+// same 16-byte phase and a thread owns the same columns in each of them: gamma
+// (or 1 + w) sits in registers (forward) or in shared memory per vector slot
+// (backward), and the backward's dgamma sums stay in registers. Outputs with the same 16-byte phase as x get 16-byte
 // stores for vectors that lie wholly inside the row and element stores at the
 // row's two ends (never touching a neighbour's elements); outputs with another
 // phase are written element by element.
@@ -23,12 +25,11 @@
 namespace rmsnorm {
 
 template <int DT, int KV, bool OFFSET>
-__global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kScalarThreads, (rowvec::FwdMinBlocks<KV>::value))
+    fwd_rowvec_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
-    extern __shared__ __align__(16) unsigned char smem[];
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma by rowvec::pad_col(column)
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -42,16 +43,30 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     const char* xb = static_cast<const char*>(a.x);
     const char* xe = xb + static_cast<size_t>(a.M - 1) * xp + rowb;  // last byte of the tensor + 1
     char* yb = static_cast<char*>(a.y);
+    // The grid is a multiple of the number of 16-byte phases x rows cycle
+    // through, so every row of this block (blockIdx.x + k * gridDim.x) starts at
+    // the same phase o and each thread owns the same columns in all of them.
+    const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(blockIdx.x) * xp) & 15);
+    const int nvr = static_cast<int>(rowb / 16) + 2;  // vectors spanned by any row
     griddep_wait();
 
-    for (int c = tid; c < N; c += nt) {
-        const float w = E::ld(a.gamma, c);
-        gsm[rowvec::pad_col(c)] = OFFSET ? 1.0f + w : w;
+    // this thread's columns of gamma (or 1 + w), in registers; 0 outside the row
+    float gf[KV][VEC];
+    unsigned full_mask = 0;  // bit k: vector k lies wholly inside the row
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        const int c0 = (16 * idx - o) / S;
+        if (idx < nvr && c0 >= 0 && c0 + VEC <= N) full_mask |= 1u << k;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int c = c0 + e;
+            const bool in = idx < nvr && c >= 0 && c < N;
+            const float w = in ? E::ld(a.gamma, c) : 0.f;
+            gf[k][e] = in ? (OFFSET ? 1.0f + w : w) : 0.f;
+        }
     }
-    __syncthreads();
 
-    // vectors spanned by any row: at most rowb/16 + 2 (bounds the store loop)
-    const int nvr = static_cast<int>(rowb / 16) + 2;
     uint4 cur[KV], nxt[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) rowvec::load_row<DT, KV>(xb, row, xp, rowb, nt, tid, xb, xe, cur);
@@ -59,9 +74,6 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
     for (; row < a.M; row += gridDim.x, parity ^= 1) {
         const int64_t next = row + gridDim.x;
         if (next < a.M) rowvec::load_row<DT, KV>(xb, next, xp, rowb, nt, tid, xb, xe, nxt);
-        const char* rb = xb + static_cast<size_t>(row) * xp;
-        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // row's byte phase
-        // column of element 0 of vector idx: (16*idx - o) / S
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
@@ -88,21 +100,14 @@ __global__ void __launch_bounds__(kScalarThreads) fwd_rowvec_kernel(const RowArg
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float f[VEC], out[VEC];
             E::unpack(cur[k], f);
-            bool full = true;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                const bool in = c >= 0 && c < N;
-                full = full && in;
-                const float g = in ? gsm[rowvec::pad_col(c)] : 0.f;
-                out[e] = OFFSET ? (g * f[e]) * r : (f[e] * r) * g;
-            }
-            if (full && same_phase) {
+            for (int e = 0; e < VEC; ++e) out[e] = OFFSET ? (gf[k][e] * f[e]) * r : (f[e] * r) * gf[k][e];
+            if (((full_mask >> k) & 1u) && same_phase) {
                 stg128(ya0 + 16 * idx, E::pack(out));
             } else {
+                const int c0 = (16 * idx - o) / S;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     const int c = c0 + e;
@@ -122,9 +127,6 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     constexpr int VEC = E::kVec;
     constexpr int S = E::kBytes;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int padded = rowvec::pad_col(a.N) + 1;
-    float* gsm = reinterpret_cast<float*>(smem);  // gamma (or 1 + w) by rowvec::pad_col(column)
-    float* acc = gsm + padded;                    // dgamma accumulators by rowvec::pad_col(column)
     __shared__ float red[2][32];
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -141,16 +143,39 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     const char* db = static_cast<const char*>(a.dy);
     const char* de = db + static_cast<size_t>(a.M - 1) * dp + rowb;
     char* dxb = static_cast<char*>(a.dx);
+    // every row of this block starts at the same 16-byte phase (see the forward);
+    // dy rows share it (same pointer phase, pitches equal modulo 16 bytes)
+    const int o = static_cast<int>(reinterpret_cast<uintptr_t>(xb + static_cast<size_t>(blockIdx.x) * xp) & 15);
+    const int nvr = static_cast<int>(rowb / 16) + 2;
+    // gamma (or 1 + w) of this block's vector slots as VEC/4 planes of float4:
+    // a warp reads 512 consecutive bytes per plane; 0 outside the row
+    float4* gsm4 = reinterpret_cast<float4*>(smem);
     griddep_wait();
-
-    for (int c = tid; c < N; c += nt) {
-        const float w = E::ld(a.gamma, c);
-        gsm[rowvec::pad_col(c)] = OFFSET ? 1.0f + w : w;
-        acc[rowvec::pad_col(c)] = 0.f;
+    for (int idx = tid; idx < nvr; idx += nt) {
+        const int c0 = (16 * idx - o) / S;
+        float w[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int c = c0 + e;
+            const bool in = c >= 0 && c < N;
+            const float v = in ? E::ld(a.gamma, c) : 0.f;
+            w[e] = in ? (OFFSET ? 1.0f + v : v) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < VEC; q += 4) gsm4[(q / 4) * nvr + idx] = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+    }
+    unsigned full_mask = 0;
+    float acc[KV][VEC];
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        const int c0 = (16 * idx - o) / S;
+        if (idx < nvr && c0 >= 0 && c0 + VEC <= N) full_mask |= 1u << k;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[k][e] = 0.f;
     }
     __syncthreads();
 
-    const int nvr = static_cast<int>(rowb / 16) + 2;
     uint4 cx[KV], cd[KV], nx[KV], nd[KV];
     int64_t row = blockIdx.x;
     if (row < a.M) {
@@ -167,25 +192,24 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
             rowvec::load_row<DT, KV>(db, next, dp, rowb, nt, tid, db, de, nd);
             r_next = __ldg(a.rstd_in + next);
         }
-        const char* rb = xb + static_cast<size_t>(row) * xp;
-        const int o = static_cast<int>(reinterpret_cast<uintptr_t>(rb) & 15);  // dy rows share it
+        // elements outside the row are zero in x and dy, and gamma is zero there
         float p0 = 0.f, p1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float xf[VEC], df[VEC];
             E::unpack(cx[k], xf);
             E::unpack(cd[k], df);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                if (c >= 0 && c < N) {
-                    const int sc = rowvec::pad_col(c);
-                    const float u = __fmul_rn(df[e], gsm[sc]);
-                    if (e & 1) p1 = fmaf(u, xf[e], p1); else p0 = fmaf(u, xf[e], p0);
-                    acc[sc] = fmaf(__fmul_rn(df[e], xf[e]), r, acc[sc]);
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 g4 = gsm4[(q / 4) * nvr + idx];
+                const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float u = __fmul_rn(df[q + e], g[e]);
+                    if (e & 1) p1 = fmaf(u, xf[q + e], p1); else p0 = fmaf(u, xf[q + e], p0);
+                    acc[k][q + e] = fmaf(__fmul_rn(df[q + e], xf[q + e]), r, acc[k][q + e]);
                 }
             }
         }
@@ -204,22 +228,21 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + k * nt;
             if (idx >= nvr) continue;
-            const int c0 = (16 * idx - o) / S;
             float xf[VEC], df[VEC], out[VEC];
             E::unpack(cx[k], xf);
             E::unpack(cd[k], df);
-            bool full = true;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = c0 + e;
-                const bool in = c >= 0 && c < N;
-                full = full && in;
-                const float u = __fmul_rn(df[e], in ? gsm[rowvec::pad_col(c)] : 0.f);
-                out[e] = fmaf(-xf[e], kk, __fmul_rn(r, u));
+            for (int q = 0; q < VEC; q += 4) {
+                const float4 g4 = gsm4[(q / 4) * nvr + idx];
+                const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    out[q + e] = fmaf(-xf[q + e], kk, __fmul_rn(r, __fmul_rn(df[q + e], g[e])));
             }
-            if (full && same_phase) {
+            if (((full_mask >> k) & 1u) && same_phase) {
                 stg128(da0 + 16 * idx, E::pack(out));
             } else {
+                const int c0 = (16 * idx - o) / S;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     const int c = c0 + e;
@@ -234,10 +257,19 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
         }
     }
     griddep_launch_dependents();
-    __syncthreads();  // the last row's accumulator updates are done
-    if (blockIdx.x < a.M) {
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
-        for (int c = tid; c < N; c += nt) wrow[c] = acc[rowvec::pad_col(c)];
+    // one row of dgamma partials per block (zeros for a block without rows): the
+    // vector slots of one phase tile the row, so every column is written once
+    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+        const int idx = tid + k * nt;
+        if (idx >= nvr) continue;
+        const int c0 = (16 * idx - o) / S;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const int c = c0 + e;
+            if (c >= 0 && c < N) wrow[c] = acc[k][e];
+        }
     }
 }
 

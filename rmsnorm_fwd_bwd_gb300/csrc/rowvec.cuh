@@ -82,5 +82,11 @@ __device__ __forceinline__ void load_row(const char* base, int64_t row, size_t p
 // banks whatever the row's phase.
 __device__ __forceinline__ int pad_col(int c) { return c + (c >> 3); }
 
+// Minimum resident blocks passed to the forward kernels' __launch_bounds__ (0:
+// none). Up to three vectors per thread the forwards fit 80 registers without
+// spills when asked for three 256-thread blocks (four of the 192-thread blocks
+// a bf16 row of 4099 gets); left alone ptxas uses 100-127 (two blocks).
+template <int KV> struct FwdMinBlocks { static constexpr int value = KV <= 3 ? 3 : 0; };
+
 }  // namespace rowvec
 }  // namespace rmsnorm
