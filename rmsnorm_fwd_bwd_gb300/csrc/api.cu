@@ -320,6 +320,75 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     return true;
 }
 
+// Ragged TMA path (RMSNorm): rows off 16 bytes whose aligned span fits one
+// ring stage of at most kSliceMaxBytes + 32 bytes; every row of a block shares
+// one phase (grid a multiple of kRowVecPhases), as on the row-vector path.
+bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    if (pass != 0 && pass != 1) return false;
+    const int s = elem_bytes(dt);
+    const int vec = 16 / s;
+    const int64_t rowb = static_cast<int64_t>(N) * s;
+    const int64_t stride = (rowb + 31) / 16 * 16;  // a ring stage: the widest span of any phase
+    if (stride > kSliceMaxBytes + 32) return false;
+    const int nslot = static_cast<int>(stride / 16);
+    const Override& ov = g_override[pass];
+    int vpt = ov.vpt;
+    int threads = ov.threads;
+    if (vpt == 0) {
+        for (vpt = 1; vpt <= 6; ++vpt) {
+            if (vpt < 2 && nslot > 32) continue;  // at least two vectors per thread unless the row is tiny
+            if (round_up(ceil_div(nslot, vpt), 32) <= kTmaMaxThreads) break;
+        }
+        if (vpt > 6 || (pass == 1 && vpt * vec > kMaxElemsPerThread[1])) return false;
+    }
+    if (vpt < 1 || vpt > 6) return false;
+    if (!threads) threads = static_cast<int>(round_up(ceil_div(nslot, vpt), 32));
+    if (threads < 32 || threads % 32 != 0 || threads > kTmaMaxThreads ||
+        static_cast<int64_t>(threads) * vpt < nslot)
+        return false;
+    p.path = kPathRagged;
+    p.dtype = dt;
+    p.offset = offset;
+    p.cluster = 1;
+    p.threads = threads;
+    p.per_thread = vpt;
+    const void* k = ragged_kernel(pass, p);
+    if (!k || !prepare_kernel(k, dev, di)) return false;
+    const int64_t stage = (pass == 0 ? 1 : 2) * stride;
+    const int64_t fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : static_cast<int64_t>(nslot) * vec * 4);
+    int bps = ov.blocks_per_sm;
+    int stages = ov.stages;
+    if (pass == 0) {
+        if (!stages) stages = 2;
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[0], 2 * stage), 2),
+                                                           kMaxBlocksPerSm));
+    } else {
+        if (!bps) {
+            bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (2 * stage), 1), 4));
+            int fit = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, threads, static_cast<size_t>(stage + 8 + fixed)) ==
+                    cudaSuccess && fit >= 1 && fit < bps)
+                bps = fit;
+        }
+        if (!stages)
+            stages = static_cast<int>(
+                std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (static_cast<int64_t>(bps) * stage), 2), 4));
+    }
+    while (stages > 1 && stages * (stage + 8) + fixed > di.smem_optin) --stages;
+    if (stages < 1) return false;
+    p.stages = stages;
+    p.smem = static_cast<size_t>(stages * (stage + 8) + fixed);
+    int64_t units = 0;
+    if (!occupancy_units(k, p, di, bps, units)) return false;
+    if (pass == 1) {
+        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
+        if (units > cap) units = cap;
+    }
+    units = std::max<int64_t>(kRowVecPhases, units / kRowVecPhases * kRowVecPhases);
+    p.units = std::min<int64_t>(units, round_up(M, kRowVecPhases));
+    return true;
+}
+
 // layout: kLayoutAligned (x, y/dy/dx and gamma 16-byte aligned), kLayoutPhase
 // (x and, for the backward, dy share a 16-byte phase), kLayoutMixed (anything else).
 enum Layout : int { kLayoutMixed = 0, kLayoutAligned = 1, kLayoutPhase = 2 };
@@ -339,7 +408,14 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     }
     bool ok = false;
     if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
-    else if (path == kPathRowVec) ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);
+    else if (path == kPathRowVec) {
+        // RMSNorm: the ragged TMA ring first, the row-vector kernels for wider rows
+        ok = pass < 2 && plan_ragged(pass, M, N, dt, offset, dev, di, p);
+        if (!ok) {
+            (void)cudaGetLastError();
+            ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);
+        }
+    }
     if (!ok && path != kPathScalar) {
         (void)cudaGetLastError();
         path = kPathScalar;  // rows too wide for the row-vector kernels, or no TMA shape
@@ -791,6 +867,9 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
     if (p.path == kPathRowVec)
         snprintf(buf, buf_len, "rowvec threads=%d kv=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
                  static_cast<long long>(p.units), p.smem, di->sms);
+    else if (p.path == kPathRagged)
+        snprintf(buf, buf_len, "ragged threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.threads,
+                 p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
     else if (p.path == kPathTma)
         snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.cluster,
                  p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);

@@ -33,7 +33,7 @@ struct RowArgs {
     uint32_t* err;         // device error word
 };
 
-enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2 };
+enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2, kPathRagged = 3 };
 
 // Most 16-byte vectors per thread on the row-vector path (256 threads).
 constexpr int kRowVecMaxKv = 5;
@@ -65,6 +65,7 @@ struct Plan {
 const void* fwd_kernel(const Plan& p);
 const void* bwd_kernel(const Plan& p);
 const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backward
+const void* ragged_kernel(int pass, const Plan& p);  // TMA ring for rows off 16 bytes; pass 0 or 1
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
