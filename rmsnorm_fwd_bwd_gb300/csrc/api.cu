@@ -320,11 +320,17 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     return true;
 }
 
-// Ragged TMA path (RMSNorm): rows off 16 bytes whose aligned span fits one
-// ring stage of at most kSliceMaxBytes + 32 bytes; every row of a block shares
-// one phase (grid a multiple of kRowVecPhases), as on the row-vector path.
+// Ragged TMA path (RMSNorm and LayerNorm): rows off 16 bytes whose aligned span
+// fits one ring stage of at most kSliceMaxBytes + 32 bytes; every row of a block
+// shares one phase (grid a multiple of kRowVecPhases), as on the row-vector path.
 bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
-    if (pass != 0 && pass != 1) return false;
+    if (pass < 0 || pass > 3) return false;
+    const int dir = pass & 1;
+    // backward: elements per thread held in registers (LayerNorm: x_hat, u and
+    // two accumulators per element)
+    const int max_elems = pass == 3 ? 24 : kMaxElemsPerThread[1];
+    // fp32 planes per vector slot in shared memory: none, gamma, gamma and beta, gamma
+    const int planes[4] = {0, 1, 2, 1};
     const int s = elem_bytes(dt);
     const int vec = 16 / s;
     const int64_t rowb = static_cast<int64_t>(N) * s;
@@ -339,7 +345,7 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
             if (vpt < 2 && nslot > 32) continue;  // at least two vectors per thread unless the row is tiny
             if (round_up(ceil_div(nslot, vpt), 32) <= kTmaMaxThreads) break;
         }
-        if (vpt > 6 || (pass == 1 && vpt * vec > kMaxElemsPerThread[1])) return false;
+        if (vpt > 6 || (dir == 1 && vpt * vec > max_elems)) return false;
     }
     if (vpt < 1 || vpt > 6) return false;
     if (!threads) threads = static_cast<int>(round_up(ceil_div(nslot, vpt), 32));
@@ -352,19 +358,20 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.cluster = 1;
     p.threads = threads;
     p.per_thread = vpt;
-    const void* k = ragged_kernel(pass, p);
+    const void* k = pass < 2 ? ragged_kernel(pass, p) : ln_ragged_kernel(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
-    const int64_t stage = (pass == 0 ? 1 : 2) * stride;
-    const int64_t fixed = 2 * 32 * 4 + 16 + (pass == 0 ? 0 : static_cast<int64_t>(nslot) * vec * 4);
+    const int64_t stage = kInputs[pass] * stride;
+    const int64_t fixed =
+        2 * kPartials[pass] * 32 * 4 + 16 + static_cast<int64_t>(planes[pass]) * nslot * vec * 4;
     int bps = ov.blocks_per_sm;
     int stages = ov.stages;
-    if (pass == 0) {
+    if (dir == 0) {
         if (!stages) stages = 2;
-        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[0], 2 * stage), 2),
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[pass], 2 * stage), 2),
                                                            kMaxBlocksPerSm));
     } else {
         if (!bps) {
-            bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (2 * stage), 1), 4));
+            bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
             int fit = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, threads, static_cast<size_t>(stage + 8 + fixed)) ==
                     cudaSuccess && fit >= 1 && fit < bps)
@@ -372,7 +379,7 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
         }
         if (!stages)
             stages = static_cast<int>(
-                std::min<int64_t>(std::max<int64_t>(kRingPerSm[1] / (static_cast<int64_t>(bps) * stage), 2), 4));
+                std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (static_cast<int64_t>(bps) * stage), 2), 4));
     }
     while (stages > 1 && stages * (stage + 8) + fixed > di.smem_optin) --stages;
     if (stages < 1) return false;
@@ -380,7 +387,7 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.smem = static_cast<size_t>(stages * (stage + 8) + fixed);
     int64_t units = 0;
     if (!occupancy_units(k, p, di, bps, units)) return false;
-    if (pass == 1) {
+    if (dir == 1) {
         const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
         if (units > cap) units = cap;
     }
@@ -409,8 +416,8 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     bool ok = false;
     if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
     else if (path == kPathRowVec) {
-        // RMSNorm: the ragged TMA ring first, the row-vector kernels for wider rows
-        ok = pass < 2 && plan_ragged(pass, M, N, dt, offset, dev, di, p);
+        // the ragged TMA ring first, the row-vector kernels for wider rows
+        ok = pass < 4 && plan_ragged(pass, M, N, dt, offset, dev, di, p);
         if (!ok) {
             (void)cudaGetLastError();
             ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);

@@ -66,6 +66,7 @@ const void* fwd_kernel(const Plan& p);
 const void* bwd_kernel(const Plan& p);
 const void* rowvec_kernel(int pass, const Plan& p);  // pass 0 forward, 1 backward
 const void* ragged_kernel(int pass, const Plan& p);  // TMA ring for rows off 16 bytes; pass 0 or 1
+const void* ln_ragged_kernel(int pass, const Plan& p);  // the same for LayerNorm; pass 2 or 3
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward

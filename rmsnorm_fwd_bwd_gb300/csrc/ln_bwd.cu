@@ -318,6 +318,7 @@ static const void* ln_bwd_for(const Plan& p) {
 
 const void* ln_bwd_kernel(const Plan& p) {
     if (p.path == kPathRowVec) return ln_rowvec_kernel(3, p);
+    if (p.path == kPathRagged) return ln_ragged_kernel(3, p);
     switch (p.dtype) {
     case kF32: return ln_bwd_for<kF32>(p);
     case kF16: return ln_bwd_for<kF16>(p);

@@ -86,12 +86,11 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
             E::unpack(idx < nvec ? __ldg(bs + idx) : make_uint4(0, 0, 0, 0), bf[v]);
         }
     }
-    // elements this warp owns in every row (a multiple of VEC), and its reciprocal
+    // elements this warp owns in every row (a multiple of VEC)
     int mine = 0;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) mine += (v * nt + tid < nvec) ? VEC : 0;
     const float n_warp = warp_allsum(static_cast<float>(mine));
-    const float inv_n_warp = n_warp > 0.f ? 1.0f / n_warp : 0.f;
 
     __syncthreads();
     if (CLUSTER) cluster_sync();  // peers' shared memory is live before any DSMEM read
@@ -131,7 +130,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
                 s1 += xf[v][e + 1];
             }
         }
-        const float m_warp = warp_allsum(s0 + s1) * inv_n_warp;
+        // a true division: equal elements give back their value exactly
+        const float m_warp = n_warp > 0.f ? warp_allsum(s0 + s1) / n_warp : 0.f;
         float q0 = 0.f, q1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -301,6 +301,7 @@ static const void* ln_fwd_for(const Plan& p) {
 
 const void* ln_fwd_kernel(const Plan& p) {
     if (p.path == kPathRowVec) return ln_rowvec_kernel(2, p);
+    if (p.path == kPathRagged) return ln_ragged_kernel(2, p);
     switch (p.dtype) {
     case kF32: return ln_fwd_for<kF32>(p);
     case kF16: return ln_fwd_for<kF16>(p);

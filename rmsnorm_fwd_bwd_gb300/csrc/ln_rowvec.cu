@@ -84,7 +84,6 @@ __global__ void __launch_bounds__(kScalarThreads, (rowvec::FwdMinBlocks<KV>::val
             }
     }
     const float n_warp = warp_allsum(static_cast<float>(cnt));
-    const float inv_n_warp = n_warp > 0.f ? 1.0f / n_warp : 0.f;
     __syncthreads();
 
     uint4 cur[KV], nxt[KV];
@@ -106,7 +105,8 @@ __global__ void __launch_bounds__(kScalarThreads, (rowvec::FwdMinBlocks<KV>::val
                 s1 += f[e + 1];
             }
         }
-        const float m_warp = warp_allsum(s0 + s1) * inv_n_warp;
+        // a true division: equal elements give back their value exactly
+        const float m_warp = n_warp > 0.f ? warp_allsum(s0 + s1) / n_warp : 0.f;
         float q0 = 0.f, q1 = 0.f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {

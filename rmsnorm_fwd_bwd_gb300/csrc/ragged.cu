@@ -20,54 +20,9 @@
 // aligned TMA kernels.
 #include "device.cuh"
 #include "launch.h"
+#include "ragged.cuh"
 
 namespace rmsnorm {
-
-namespace {
-
-// 16-byte mask keeping the elements whose bits are set in `bits` (bit e: element e).
-template <int DT>
-__device__ __forceinline__ uint4 keep_mask(unsigned bits) {
-    uint32_t w[4];
-    if (Elem<DT>::kBytes == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = ((bits >> i) & 1u) ? 0xffffffffu : 0u;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = (((bits >> (2 * i)) & 1u) ? 0x0000ffffu : 0u) | (((bits >> (2 * i + 1)) & 1u) ? 0xffff0000u : 0u);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Slot idx of a row at phase o: its elements e with column c0 + e inside [0, N).
-template <int DT>
-__device__ __forceinline__ unsigned slot_bits(int idx, int nv, int o, int N, int& c0) {
-    constexpr int VEC = Elem<DT>::kVec;
-    c0 = (16 * idx - o) / Elem<DT>::kBytes;
-    unsigned bits = 0u;
-    if (idx < nv) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            if (c0 + e >= 0 && c0 + e < N) bits |= 1u << e;
-    }
-    return bits;
-}
-
-// Load slot idx of a stage and zero the elements outside the row.
-template <int DT>
-__device__ __forceinline__ uint4 slot_load(const unsigned char* st, int idx, unsigned bits) {
-    constexpr unsigned kAll = (1u << Elem<DT>::kVec) - 1u;
-    if (bits == 0u) return make_uint4(0, 0, 0, 0);
-    uint4 v = *reinterpret_cast<const uint4*>(st + idx * 16);
-    if (bits != kAll) {
-        const uint4 m = keep_mask<DT>(bits);
-        v.x &= m.x; v.y &= m.y; v.z &= m.z; v.w &= m.w;
-    }
-    return v;
-}
-
-}  // namespace
 
 // Minimum resident blocks passed to the forward's __launch_bounds__ (0: none):
 // these instances fit 68 registers without spills when asked for three
@@ -120,7 +75,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (RaggedFwdMinBlocks<DT, VPT>::
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         int c0;
-        bits[v] = slot_bits<DT>(v * nt + tid, nv, o, N, c0);
+        bits[v] = ragged::slot_bits<DT>(v * nt + tid, nv, o, N, c0);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             const bool in = (bits[v] >> e) & 1u;
@@ -154,7 +109,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (RaggedFwdMinBlocks<DT, VPT>::
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
-            E::unpack(slot_load<DT>(st, v * nt + tid, bits[v]), xf[v]);
+            E::unpack(ragged::slot_load<DT>(st, v * nt + tid, bits[v]), xf[v]);
 #pragma unroll
             for (int e = 0; e < VEC; e += 2) {
                 ss0 = fmaf(xf[v][e], xf[v][e], ss0);
@@ -258,7 +213,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
     // gamma (or 1 + w) by vector slot at this block's phase, zero outside the row
     for (int idx = tid; idx < nslot; idx += nt) {
         int c0;
-        const unsigned b = slot_bits<DT>(idx, nv, o, N, c0);
+        const unsigned b = ragged::slot_bits<DT>(idx, nv, o, N, c0);
         float w[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -274,7 +229,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         int c0;
-        bits[v] = slot_bits<DT>(v * nt + tid, nv, o, N, c0);
+        bits[v] = ragged::slot_bits<DT>(v * nt + tid, nv, o, N, c0);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
     }
@@ -317,8 +272,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
             float df[VEC];
-            E::unpack(slot_load<DT>(st, idx, bits[v]), xf[v]);
-            E::unpack(slot_load<DT>(st + stride, idx, bits[v]), df);
+            E::unpack(ragged::slot_load<DT>(st, idx, bits[v]), xf[v]);
+            E::unpack(ragged::slot_load<DT>(st + stride, idx, bits[v]), df);
             float g[VEC];
             if (bits[v]) {
 #pragma unroll

@@ -3,8 +3,8 @@ the CPU oracle.
 
 Every case gates y, mean, rstd, dx, dgamma and dbeta with the golden /
 reference / target gate. Shapes cover the TMA path (one CTA per row slice),
-the cluster path (rows split over 2 and 4 CTAs), the row-vector path (ragged or
-misaligned rows), the general path (rows over 20 KB that are not 16-byte
+the cluster path (rows split over 2 and 4 CTAs), the ragged TMA path (rows off
+16 bytes up to 16 KB), the row-vector path (such rows of 16-20 KB), the general path (rows over 20 KB that are not 16-byte
 multiples, x and dy at different 16-byte phases), tiny and empty inputs, rows with a large mean (where a
 one-pass variance would cancel), constant rows (variance 0), strided rows, and
 the measured LayerNorm workloads at full size on sampled rows.
@@ -62,8 +62,9 @@ SHAPES = [
     ("bfloat16", 40, 16384, "tma cluster=2"),
     ("float16", 33, 12288, "tma cluster=2"),
     ("float32", 24, 16384, "tma cluster=4"),
-    ("bfloat16", 67, 4099, "rowvec"),
-    ("float32", 50, 333, "rowvec"),
+    ("bfloat16", 67, 4099, "ragged"),
+    ("float32", 50, 333, "ragged"),
+    ("float32", 29, 4099, "ragged"),
     ("float16", 31, 9999, "rowvec"),
     ("float32", 29, 6001, "scalar"),
     ("bfloat16", 23, 16383, "scalar"),
@@ -84,7 +85,7 @@ def test_misaligned_pointers(dtype):
     # only the outputs off (row-vector path, element stores); x off but dy not
     # (the backward's general path)
     M, N = 45, 2048
-    assert _plan(2, M, N, dtype, 0).startswith("rowvec") and _plan(3, M, N, dtype, 0).startswith("rowvec")
+    assert _plan(2, M, N, dtype, 0).startswith("ragged") and _plan(3, M, N, dtype, 0).startswith("ragged")
     assert _plan(3, M, N, dtype, 2).startswith("scalar")
     x, g, b, dy = inputs.make_ln_inputs(M, N, dtype, seed=11)
     _gate(x, g, b, dy, dtype, misalign=True, title=f"layernorm {dtype} misaligned")
@@ -117,7 +118,7 @@ def test_large_row_means(dtype, N):
     _gate(x, g, b, dy, dtype, title=f"layernorm {dtype} N={N} large means")
 
 
-@pytest.mark.parametrize("dtype,N", [("bfloat16", 4096), ("float32", 8192), ("float16", 1001)])
+@pytest.mark.parametrize("dtype,N", [("bfloat16", 4096), ("float32", 8192), ("float16", 1001), ("float16", 1000)])
 def test_constant_rows(dtype, N):
     # values on a 1/16 grid: every partial sum is exact, so the mean is the row's
     # value, x_hat = 0 exactly, y = beta and dgamma = 0
