@@ -70,8 +70,18 @@ def gate_outputs(x, g, dy, dtype, offset, eps, y=None, rstd=None, dx=None, dgamm
             xc = orc.decode(np.ascontiguousarray(x[:, col]), dtype)
             dyc = orc.decode(np.ascontiguousarray(dy[:, col]), dtype)
             cond = gate.condition_number(dyc * xc * rfull)
-        out.append(gate.check("dgamma", dgg, orc.decode(dgr, dtype), tgt, dtype, rel_bound=rel,
-                              condition=cond))
+        res = gate.check("dgamma", dgg, orc.decode(dgr, dtype), tgt, dtype, rel_bound=rel, condition=cond)
+        # report-only: the same terms summed pairwise over rows (a second fp32 reference)
+        pw = orc.decode(orc.dgamma_pairwise_reference(dy, x, g, dtype, eps=eps, offset=offset), dtype)
+        finite = np.isfinite(dgg)
+        if finite.any() and np.isfinite(res.target_error):
+            pw_err = float(np.max(np.abs(pw[finite] - dgg[finite])))
+            within = res.target_error <= gate.FUDGE_FACTOR * pw_err + res.absolute_floor
+            res.notes.append(f"pairwise fp32 reference error {pw_err:.3e} (sequential {res.reference_error:.3e}); "
+                             f"target {'within' if within else 'outside'} the gate built on it")
+            res.pairwise_error = pw_err
+            res.pairwise_within = within
+        out.append(res)
     return out
 
 

@@ -58,6 +58,10 @@ class GateResult:
     gate_valid: bool = False
     verdict: str = "FAIL"
     notes: list = field(default_factory=list)
+    # report-only (dgamma): error of the pairwise-summed fp32 reference, and
+    # whether the target also meets the gate built on it
+    pairwise_error: float | None = None
+    pairwise_within: bool | None = None
 
     @property
     def passed(self) -> bool:

@@ -46,6 +46,8 @@ PARITY = {
                       "contracted with ddx and ddgamma, for dy, x and gamma (plain and offset); "
                       "linearity in (ddx, ddgamma); zero cotangents give zero",
     "bwd_bwd_reference": "pinned: brute-force fp32 loop on tiny inputs, error bound vs golden",
+    "dgamma_pairwise_reference": "pinned: brute-force fp32 pairwise loop on tiny inputs, "
+                                 "log2(M) error bound vs golden",
 }
 
 _lock = threading.Lock()
@@ -91,6 +93,7 @@ def _load():
             "oracle_ln_bwd_reference": [P, P, P, I64, I64, F, I, P, P, P],
             "oracle_bwd_bwd_golden": [P, P, P, P, P, I64, I64, D, I, I, P, P, P],
             "oracle_bwd_bwd_reference": [P, P, P, P, P, I64, I64, F, I, I, P, P, P],
+            "oracle_dgamma_pairwise_reference": [P, P, P, I64, I64, F, I, I, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -291,3 +294,15 @@ def bwd_bwd_reference(ddx, ddg, dy, x, gamma, dtype, eps=1e-6, offset=False):
     _load().oracle_bwd_bwd_reference(_ptr(ddx), _ptr(ddg), _ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps),
                                      DTYPES[dtype], int(bool(offset)), _ptr(d_dy), _ptr(d_x), _ptr(d_g))
     return d_dy, d_x, d_g
+
+
+def dgamma_pairwise_reference(dy, x, gamma, dtype, eps=1e-6, offset=False):
+    """dgamma [N] in dtype storage: fp32 terms summed over rows by a pairwise tree."""
+    x = _check(x, dtype)
+    M, N = x.shape
+    dy = _check(dy, dtype, (M, N))
+    gamma = _check(gamma, dtype, (N,))
+    dg = np.empty(N, STORAGE[dtype])
+    _load().oracle_dgamma_pairwise_reference(_ptr(dy), _ptr(x), _ptr(gamma), M, N, float(eps), DTYPES[dtype],
+                                             int(bool(offset)), _ptr(dg))
+    return dg

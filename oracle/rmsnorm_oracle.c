@@ -625,3 +625,43 @@ void oracle_bwd_bwd_reference(const void* ddx, const void* ddg, const void* dy, 
         for (int64_t j = 0; j < N; ++j) store_elem(d_gamma, j, dt, (double)acc[j]);
     free(acc);
 }
+
+/* ------------------------------------------------------------------------- */
+/* dgamma with pairwise row sums (a report-only second reference)             */
+/* ------------------------------------------------------------------------- */
+
+/* fp32 pairwise (recursive halving) sum of t[lo .. hi). */
+static float pairwise_sum_f32(const float* t, int64_t lo, int64_t hi) {
+    const int64_t n = hi - lo;
+    if (n <= 0) return 0.0f;
+    if (n == 1) return t[lo];
+    const int64_t mid = lo + n / 2;
+    const float a = pairwise_sum_f32(t, lo, mid);
+    const float b = pairwise_sum_f32(t, mid, hi);
+    return a + b;
+}
+
+/*
+ * dgamma[N] in dtype dt: the same fp32 terms as oracle_bwd_reference,
+ * (dy * x) * r with r recomputed in fp32 per row, but summed over the rows by a
+ * pairwise tree (error growing with log2 M rather than M), rounded once. The
+ * gate reports the target's distance from it next to the sequential reference
+ * (the pages leave the summation order of the reference open).
+ */
+void oracle_dgamma_pairwise_reference(const void* dy, const void* x, const void* gamma, int64_t M, int64_t N,
+                                      float eps, int dt, int offset, void* dgamma) {
+    (void)gamma;
+    (void)offset;  /* dgamma has the same formula with and without the offset */
+    float* r = (float*)malloc((size_t)(M > 0 ? M : 1) * sizeof(float));
+    float* t = (float*)malloc((size_t)(M > 0 ? M : 1) * sizeof(float));
+    for (int64_t i = 0; i < M; ++i) r[i] = row_rstd_f32(x, i * N, N, eps, dt);
+    for (int64_t j = 0; j < N; ++j) {
+        for (int64_t i = 0; i < M; ++i) {
+            const float dyx = ld32(dy, i * N + j, dt) * ld32(x, i * N + j, dt);
+            t[i] = dyx * r[i];
+        }
+        store_elem(dgamma, j, dt, (double)pairwise_sum_f32(t, 0, M));
+    }
+    free(r);
+    free(t);
+}

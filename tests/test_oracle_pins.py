@@ -378,3 +378,41 @@ def test_offset_equals_plain_with_one_plus_w(dtype):
     dxp, dgp = orc.bwd_golden(dy, x, gs, dtype, offset=False)
     np.testing.assert_allclose(dxo, dxp, rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(dgo, dgp, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+# the report-only pairwise dgamma reference
+# --------------------------------------------------------------------------- #
+def _pairwise(t):
+    f32 = np.float32
+    if len(t) == 0:
+        return f32(0)
+    if len(t) == 1:
+        return t[0]
+    mid = len(t) // 2
+    return f32(_pairwise(t[:mid]) + _pairwise(t[mid:]))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_pairwise_dgamma_reference_brute_force(dtype):
+    f32 = np.float32
+    M, N = 7, 3
+    x, gam, dy = inputs.make_inputs(M, N, dtype, seed=51)
+    xv = orc.decode(x, dtype).astype(np.float32)
+    dyv = orc.decode(dy, dtype).astype(np.float32)
+    _, r = orc.fwd_reference(x, gam, dtype)
+    want = np.array([_pairwise([f32(f32(dyv[i, j] * xv[i, j]) * r[i]) for i in range(M)]) for j in range(N)],
+                    np.float32)
+    np.testing.assert_array_equal(orc.dgamma_pairwise_reference(dy, x, gam, dtype), inputs.to_storage(want, dtype))
+
+
+def test_pairwise_dgamma_reference_error_bound():
+    # pairwise summation: error <= ceil(log2 M) * u32 * sum|terms| (plus the terms' own rounding)
+    M, N = 3000, 64
+    x, gam, dy = inputs.make_inputs(M, N, "float32", seed=52)
+    _, dgg = orc.bwd_golden(dy, x, gam, "float32", want_dx=False)
+    pw = orc.dgamma_pairwise_reference(dy, x, gam, "float32").astype(np.float64)
+    _, r = orc.fwd_golden(x, gam, "float32")
+    mag = np.sum(np.abs(dy.astype(np.float64) * x.astype(np.float64) * r[:, None]), axis=0)
+    u32 = 2.0 ** -24
+    assert np.all(np.abs(pw - dgg) <= (math.ceil(math.log2(M)) + 4 + N) * u32 * mag)
