@@ -56,6 +56,7 @@ constexpr int kColumnPlanes[kPasses] = {0, 1, 0, 1, 2};
 constexpr int kMaxElemsPerThread[kPasses] = {0, 32, 0, 16, 16};
 constexpr int kRingPerSm[kPasses] = {48 << 10, 96 << 10, 64 << 10, 96 << 10, 96 << 10};
 constexpr int kMaxBlocksPerSm = 16;
+constexpr int kRaggedFwdRingPerSm = 64 << 10;
 // Rows split over a cluster pay a cluster barrier per row; there a third
 // RMSNorm forward stage and more resident blocks hide it better (measured; the
 // LayerNorm forward, with more registers per thread, is faster with two).
@@ -366,8 +367,10 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     int bps = ov.blocks_per_sm;
     int stages = ov.stages;
     if (dir == 0) {
+        // the ragged forwards are latency-bound at low occupancy: a 64 KB ring per SM
+        // (bf16 N = 4099: 4 blocks, 5836 GB/s at 65536 rows, against 5024 with 3)
         if (!stages) stages = 2;
-        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRingPerSm[pass], 2 * stage), 2),
+        if (!bps) bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(ceil_div(kRaggedFwdRingPerSm, 2 * stage), 2),
                                                            kMaxBlocksPerSm));
     } else {
         if (!bps) {
