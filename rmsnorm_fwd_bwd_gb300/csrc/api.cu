@@ -292,7 +292,7 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.offset = offset;
     p.cluster = 1;
     // as few threads as hold the row at kv vectors each: every warp then carries
-    // the same number of vectors (bf16 N = 4099: 514 vectors -> 192 threads x 3,
+    // the same number of vectors (514 vectors -> 192 threads x 3,
     // not 256 x 3 with one warp doing a third vector while the others wait at
     // the row barrier), and more blocks fit per SM
     p.threads = static_cast<int>(std::min<int64_t>(round_up(ceil_div(nvr, kv), 32), kScalarThreads));

@@ -1,7 +1,7 @@
 // ln_rowvec.cu -- LayerNorm forward and backward for rows that do not start on a
-// 16-byte boundary (N * sizeof(dtype) not a multiple of 16, e.g. bf16 N = 4099,
-// or pointers and pitches off 16 bytes), with the formulas of ln_fwd.cu and
-// ln_bwd.cu.
+// 16-byte boundary (N * sizeof(dtype) not a multiple of 16, or pointers and
+// pitches off 16 bytes) and are too wide for the ragged TMA kernels
+// (ln_ragged.cu): rows of 16-20 KB. Formulas of ln_fwd.cu and ln_bwd.cu.
 //
 // Loads as in rowvec.cu: thread t holds vectors t, t + nt, ... of the row's
 // 16-byte aligned span in registers (elements outside the row masked to zero),

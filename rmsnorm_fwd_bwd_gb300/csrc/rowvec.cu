@@ -1,6 +1,8 @@
 // rowvec.cu -- forward and backward for rows that do not start on a 16-byte
-// boundary (N * sizeof(dtype) not a multiple of 16, e.g. bf16 N = 4099), with
-// the same formulas as fwd.cu / bwd.cu.
+// boundary (N * sizeof(dtype) not a multiple of 16, or pointers and pitches off
+// 16 bytes) and are too wide for one ring stage of the ragged TMA kernels
+// (ragged.cu): rows of 16-20 KB, e.g. bf16 N = 9999. Same formulas as fwd.cu /
+// bwd.cu.
 //
 // A row starting at byte B covers the 16-byte aligned vectors from
 // floor16(B) to ceil16(B + N*s) (rows may be further apart than N elements:

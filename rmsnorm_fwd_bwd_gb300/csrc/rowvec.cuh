@@ -1,7 +1,7 @@
 // rowvec.cuh -- loads shared by the row-vector kernels (rowvec.cu for RMSNorm,
 // ln_rowvec.cu for LayerNorm): 16-byte loads of the aligned span of a row that
 // does not start on a 16-byte boundary, masked to the row and never reaching
-// outside the tensor, and the padded shared-memory slot of a column.
+// outside the tensor.
 #pragma once
 
 #include "device.cuh"
@@ -76,16 +76,10 @@ __device__ __forceinline__ void load_row(const char* base, int64_t row, size_t p
     }
 }
 
-// Shared-memory slot of column c. A thread owns 8 (or 4) consecutive columns, so
-// for one element position the 32 lanes of a warp touch columns 8 apart; one
-// padding word after every 8 columns puts those 32 accesses in 32 different
-// banks whatever the row's phase.
-__device__ __forceinline__ int pad_col(int c) { return c + (c >> 3); }
-
 // Minimum resident blocks passed to the forward kernels' __launch_bounds__ (0:
 // none). Up to three vectors per thread the forwards fit 80 registers without
-// spills when asked for three 256-thread blocks (four of the 192-thread blocks
-// a bf16 row of 4099 gets); left alone ptxas uses 100-127 (two blocks).
+// spills when asked for three 256-thread blocks (four 192-thread blocks); left
+// alone ptxas uses 100-127 (two blocks).
 template <int KV> struct FwdMinBlocks { static constexpr int value = KV <= 3 ? 3 : 0; };
 
 }  // namespace rowvec
