@@ -189,6 +189,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int, path: str):
         self.path = path
         self.proc = None
+        self.f = None
         self.gpu = gpu_index
         try:
             self.f = open(path, "w")
@@ -196,8 +197,11 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
+            if self.f is not None:
+                self.f.close()
+                self.f = None
 
     def stop(self):
         if self.proc is not None:
@@ -213,7 +217,9 @@ class ClockSampler:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue

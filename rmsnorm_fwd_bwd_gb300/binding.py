@@ -90,7 +90,8 @@ def header_functions() -> list:
     for fn in sorted(os.listdir(INCLUDE_DIR)):
         if not fn.endswith(".h"):
             continue
-        text = open(os.path.join(INCLUDE_DIR, fn)).read()
+        with open(os.path.join(INCLUDE_DIR, fn)) as f:
+            text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names.update(re.findall(r"\b((?:rmsnorm|layernorm)_[a-z0-9_]+)\s*\(", text))
     return sorted(names)

@@ -327,7 +327,8 @@ def test_float16_rounding_matches_numpy():
          3 * 2.0 ** -26, 2.0 ** -14, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, np.inf, -np.inf],
     ])
     ours = orc.encode(vals, "float16")
-    ref = vals.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # values beyond the float16 range become infinities
+        ref = vals.astype(np.float16).view(np.uint16)
     np.testing.assert_array_equal(ours, ref)
     back = orc.decode(ours, "float16")
     np.testing.assert_array_equal(back, ref.view(np.float16).astype(np.float64))
