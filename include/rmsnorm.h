@@ -200,8 +200,10 @@ rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dty
 
 /*
  * Tuning hook: override the TMA-path launch shape for one pass (0 = forward,
- * 1 = backward, 2 / 3 = LayerNorm forward / backward, 4 = double backward). threads: threads per block (multiple of 32); vpt: 16-byte
- * vectors per thread (1, 2, 4 or 8); stages: pipeline depth; blocks_per_sm:
+ * 1 = backward, 2 / 3 = LayerNorm forward / backward, 4 = double backward).
+ * threads: threads per block (multiple of 32); vpt: 16-byte vectors per thread
+ * (1 to 8; the aligned TMA path takes 1, 2, 4 or 8, the ragged one 1 to 6);
+ * stages: pipeline depth; blocks_per_sm:
  * cap on resident blocks per SM. Any value 0 keeps the built-in choice;
  * all zeros restores the defaults. A shape that cannot hold the row makes the
  * following calls fail with RMSNORM_ERR_UNSUPPORTED. Process-wide, not

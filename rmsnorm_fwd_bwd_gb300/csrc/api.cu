@@ -325,13 +325,15 @@ bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const 
 // fits one ring stage of at most kSliceMaxBytes + 32 bytes; every row of a block
 // shares one phase (grid a multiple of kRowVecPhases), as on the row-vector path.
 bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
-    if (pass < 0 || pass > 3) return false;
-    const int dir = pass & 1;
+    if (pass < 0 || pass >= kPasses) return false;
+    const int dir = kMaxElemsPerThread[pass] > 0 ? 1 : 0;
     // backward: elements per thread held in registers (LayerNorm: x_hat, u and
-    // two accumulators per element)
-    const int max_elems = pass == 3 ? 24 : kMaxElemsPerThread[1];
-    // fp32 planes per vector slot in shared memory: none, gamma, gamma and beta, gamma
-    const int planes[4] = {0, 1, 2, 1};
+    // two accumulators per element; the double backward: x, dy, ddx and one
+    // accumulator per element)
+    const int max_elems = pass >= 3 ? 24 : kMaxElemsPerThread[1];
+    // fp32 planes per vector slot in shared memory: none, gamma, gamma and beta,
+    // gamma, gamma and ddgamma
+    const int planes[kPasses] = {0, 1, 2, 1, 2};
     const int s = elem_bytes(dt);
     const int vec = 16 / s;
     const int64_t rowb = static_cast<int64_t>(N) * s;
@@ -339,18 +341,35 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     if (stride > kSliceMaxBytes + 32) return false;
     const int nslot = static_cast<int>(stride / 16);
     const Override& ov = g_override[pass];
+    const int tcap = pass == 4 ? kRaggedDbwdMaxThreads : kTmaMaxThreads;
     int vpt = ov.vpt;
     int threads = ov.threads;
-    if (vpt == 0) {
+    if (vpt == 0 && pass == 4 && vec == 4) {
+        // double backward, fp32: the fewest vectors per thread (measured: N = 4099
+        // 288 x 4 at 5562 GB/s against 5171 for 224 x 5; N = 333 96 x 1 at 4504
+        // against 3825 for 64 x 2)
+        for (vpt = 1; vpt <= 6 && round_up(ceil_div(nslot, vpt), 32) > tcap; ++vpt) {
+        }
+        if (vpt > 6 || vpt * vec > max_elems) return false;
+    } else if (vpt == 0 && pass == 4) {
+        // double backward, 2-byte types: the fewest threads at the most vectors per
+        // thread the register budget allows (measured: bf16 N = 4099 192 x 3 at 4794
+        // GB/s against 4103 for 288 x 2; N = 2051 96 x 3 at 4374 against 3816 for 160 x 2)
+        const int64_t t = round_up(ceil_div(nslot, max_elems / vec), 32);
+        if (t > tcap) return false;
+        vpt = static_cast<int>(ceil_div(nslot, t));
+    } else if (vpt == 0) {
+        // the fewest vectors per thread (at least two unless the row is tiny) whose
+        // block fits
         for (vpt = 1; vpt <= 6; ++vpt) {
-            if (vpt < 2 && nslot > 32) continue;  // at least two vectors per thread unless the row is tiny
-            if (round_up(ceil_div(nslot, vpt), 32) <= kTmaMaxThreads) break;
+            if (vpt < 2 && nslot > 32) continue;
+            if (round_up(ceil_div(nslot, vpt), 32) <= tcap) break;
         }
         if (vpt > 6 || (dir == 1 && vpt * vec > max_elems)) return false;
     }
     if (vpt < 1 || vpt > 6) return false;
     if (!threads) threads = static_cast<int>(round_up(ceil_div(nslot, vpt), 32));
-    if (threads < 32 || threads % 32 != 0 || threads > kTmaMaxThreads ||
+    if (threads < 32 || threads % 32 != 0 || threads > tcap ||
         static_cast<int64_t>(threads) * vpt < nslot)
         return false;
     p.path = kPathRagged;
@@ -359,7 +378,7 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     p.cluster = 1;
     p.threads = threads;
     p.per_thread = vpt;
-    const void* k = pass < 2 ? ragged_kernel(pass, p) : ln_ragged_kernel(pass, p);
+    const void* k = pass < 2 ? ragged_kernel(pass, p) : (pass < 4 ? ln_ragged_kernel(pass, p) : dbwd_kernel(p));
     if (!k || !prepare_kernel(k, dev, di)) return false;
     const int64_t stage = kInputs[pass] * stride;
     const int64_t fixed =
@@ -374,7 +393,12 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
                                                            kMaxBlocksPerSm));
     } else {
         if (!bps) {
-            bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
+            // the double backward holds three rows in registers and is latency-bound:
+            // as many blocks as fit (bf16 N = 4099: 2 blocks of 2 stages, 4794 GB/s
+            // at 65536 rows against 3100 with the ring rule's one; fp16 N = 1001: 10
+            // blocks, 3976 against 3057 with 4)
+            bps = pass == 4 ? kMaxBlocksPerSm
+                            : static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
             int fit = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, threads, static_cast<size_t>(stage + 8 + fixed)) ==
                     cudaSuccess && fit >= 1 && fit < bps)
@@ -409,7 +433,7 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
     if (layout == kLayoutAligned && tma_shape) path = kPathTma;
-    else if (layout != kLayoutMixed && pass != 4) path = kPathRowVec;  // no double-backward row-vector kernel
+    else if (layout != kLayoutMixed) path = kPathRowVec;
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
@@ -420,8 +444,8 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
     else if (path == kPathRowVec) {
         // the ragged TMA ring first, the row-vector kernels for wider rows
-        ok = pass < 4 && plan_ragged(pass, M, N, dt, offset, dev, di, p);
-        if (!ok) {
+        ok = plan_ragged(pass, M, N, dt, offset, dev, di, p);
+        if (!ok && pass < 4) {  // no double-backward row-vector kernel
             (void)cudaGetLastError();
             ok = plan_rowvec(pass, M, N, dt, offset, dev, di, p);
         }
@@ -701,15 +725,20 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
         !aligned(rstd, 4) || !aligned(d_dy, s) || !aligned(d_x, s) || !aligned(workspace, 16))
         return RMSNORM_ERR_ALIGN;
     // TMA path: every row and per-column pointer 16-byte aligned with 16-byte
-    // pitches; anything else: the general path
+    // pitches; ragged TMA path: rows of x, dy and ddx at one 16-byte phase (same
+    // pointer phase, pitches equal modulo 16 bytes); anything else: the general path
     const bool a16 = aligned(ddx, 16) && aligned(ddgamma, 16) && aligned(dy, 16) && aligned(x, 16) &&
                      aligned(gamma, 16) && aligned(d_dy, 16) && aligned(d_x, 16) && (ldddx * s) % 16 == 0 &&
                      (lddy * s) % 16 == 0 && (ldx * s) % 16 == 0 && (ldd_dy * s) % 16 == 0 &&
                      (ldd_x * s) % 16 == 0;
+    const uintptr_t ph = reinterpret_cast<uintptr_t>(x) & 15;
+    const bool same_phase = (reinterpret_cast<uintptr_t>(dy) & 15) == ph &&
+                            (reinterpret_cast<uintptr_t>(ddx) & 15) == ph && (ldx * s) % 16 == (lddy * s) % 16 &&
+                            (ldx * s) % 16 == (ldddx * s) % 16;
+    const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
     if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
     Plan p;
-    if (!get_plan(4, M, static_cast<int>(N), dtype, offset, a16 ? kLayoutAligned : kLayoutMixed, dev, *di, p))
-        return RMSNORM_ERR_UNSUPPORTED;
+    if (!get_plan(4, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
     const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -817,7 +846,7 @@ extern "C" size_t rmsnorm_bwd_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_d
     if (current_device(dev, di) != RMSNORM_OK) return 0;
     int64_t units = 0;
     Plan p;
-    for (int layout : {kLayoutMixed, kLayoutAligned})
+    for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
         for (int off = 0; off < 2; ++off)
             if (get_plan(4, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
                 units = p.units;
@@ -893,7 +922,7 @@ extern "C" rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int
                                                       int blocks_per_sm) {
     if (pass < 0 || pass >= kPasses) return RMSNORM_ERR_ARG;
     if (threads < 0 || threads > 1024 || threads % 32 != 0 || stages < 0 || stages > 64 || blocks_per_sm < 0 ||
-        (vpt != 0 && vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8))
+        vpt < 0 || vpt > 8)
         return RMSNORM_ERR_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
     g_override[pass].threads = threads;

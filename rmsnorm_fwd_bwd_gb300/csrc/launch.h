@@ -46,6 +46,10 @@ constexpr int kRowVecPhases = 8;
 // 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over
 // the row with 256 threads.
 constexpr int kTmaMaxThreads = 256;
+// The ragged double backward may take up to 10 warps: fp32 rows of up to 16 KB
+// then need at most four vectors per thread, bf16 rows of up to 7680 elements
+// three.
+constexpr int kRaggedDbwdMaxThreads = 320;
 constexpr int kScalarThreads = 256;
 
 // A launch shape chosen by the planner.
@@ -70,7 +74,8 @@ const void* ln_ragged_kernel(int pass, const Plan& p);  // the same for LayerNor
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
-const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA or scalar path)
+const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA, ragged or scalar path)
+const void* dbwd_ragged_kernel_ptr(const Plan& p);    // its ragged TMA kernel
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
 cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);

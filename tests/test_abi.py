@@ -67,7 +67,8 @@ def test_host_validation_without_gpu():
     assert B.rmsnorm_set_launch_override(3, 0, 0, 0, 0) == 0
     assert B.rmsnorm_set_launch_override(4, 0, 0, 0, 0) == 0
     assert B.rmsnorm_set_launch_override(0, 33, 0, 0, 0) == 9
-    assert B.rmsnorm_set_launch_override(0, 0, 3, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(0, 0, 9, 0, 0) == 9
+    assert B.rmsnorm_set_launch_override(0, 0, -1, 0, 0) == 9
     assert B.rmsnorm_set_launch_override(0, 0, 0, 0, 0) == 0
 
 

@@ -3,7 +3,9 @@ oracle, and second-order autograd through rms_norm.
 
 Every case gates d_dy, d_x and d_gamma with the golden / reference / target
 gate. Shapes cover the TMA path, the cluster path (rows over 4096 elements),
-the general path (ragged or misaligned rows), the offset variant, an absent
+the ragged TMA path (rows off 16 bytes: odd row lengths, shifted pointers,
+odd pitches, outputs at another phase), the general path (inputs at different
+phases, rows too wide for the ragged ring), the offset variant, an absent
 ddgamma, empty inputs, strided rows and the headline shape at full size on
 sampled rows.
 """
@@ -59,8 +61,14 @@ SHAPES = [
     ("float32", 41, 8192, "tma cluster=2"),
     ("bfloat16", 40, 16384, "tma cluster=4"),
     ("float32", 24, 16384, "tma cluster=4"),
-    ("bfloat16", 67, 4099, "scalar"),
-    ("float32", 50, 333, "scalar"),
+    ("bfloat16", 67, 4099, "ragged"),
+    ("float32", 50, 333, "ragged"),
+    ("float16", 33, 1001, "ragged"),
+    ("bfloat16", 9, 3, "ragged"),
+    ("float32", 19, 4099, "ragged"),
+    ("bfloat16", 20, 7001, "ragged"),
+    ("bfloat16", 20, 8001, "scalar"),
+    ("float32", 16, 5001, "scalar"),
 ]
 
 
@@ -77,8 +85,19 @@ def test_without_ddgamma(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
-def test_misaligned_pointers_take_the_general_path(dtype):
-    _gate(45, 2048, dtype, seed=11, misalign=True, title=f"double backward {dtype} misaligned")
+@pytest.mark.parametrize("offset", [False, True])
+def test_shifted_pointers_take_the_ragged_path(dtype, offset):
+    # every tensor one element off a 16-byte boundary: x, dy and ddx share a phase
+    assert _plan(45, 2048, dtype, aligned16=0).startswith("ragged")
+    _gate(45, 2048, dtype, seed=11, offset=offset, misalign=True, title=f"double backward {dtype} shifted")
+
+
+@pytest.mark.parametrize("names", [{"x"}, {"dy"}, {"ddx"}, {"d_dy"}, {"d_x"}, {"ddx", "dy", "x"}])
+@pytest.mark.parametrize("N", [2048, 4099])
+def test_partly_shifted_pointers(names, N):
+    # inputs at different phases take the general path; outputs at any phase get
+    # element stores on the ragged path
+    _gate(37, N, "bfloat16", seed=12, misalign=names, title=f"double backward shifted {sorted(names)} N={N}")
 
 
 def test_repeated_runs_are_bitwise_identical():
@@ -103,36 +122,55 @@ def test_empty_rows_zero_d_gamma():
     assert torch.all(dg == 0)
 
 
-def test_strided_rows():
+@pytest.mark.parametrize("M,N,ld,ld_out", [(67, 4096, 4160, 4160), (67, 4099, 4111, 4100), (29, 1001, 1001, 1013)])
+def test_strided_rows(M, N, ld, ld_out):
+    # pitches (elements) of the inputs and of the outputs; odd pitches put the rows
+    # of one tensor at eight different 16-byte phases
     import torch
     from rmsnorm_fwd_bwd_gb300 import binding as B
-    M, N, ld, dtype = 67, 4096, 4160, "bfloat16"
+    dtype = "bfloat16"
     x, g, dy = inputs.make_inputs(M, N, dtype, seed=21)
     ddx, ddg = _cotangents(M, N, dtype, 21)
 
-    def wide(a):
-        buf = torch.full((M, ld), 1234.0, dtype=torch.bfloat16, device="cuda")
-        buf[:, :N] = B.to_device(a.reshape(-1), dtype).view(M, N)
+    def wide(a, pitch):
+        buf = torch.full((M, pitch), 1234.0, dtype=torch.bfloat16, device="cuda")
+        if a is not None:
+            buf[:, :N] = B.to_device(a.reshape(-1), dtype).view(M, N)
         return buf
 
-    xb, dyb, tb = wide(x), wide(dy), wide(ddx)
+    xb, dyb, tb = wide(x, ld), wide(dy, ld), wide(ddx, ld)
     gt, qt = B.to_device(g, dtype), B.to_device(ddg, dtype)
     rstd = torch.empty(M, device="cuda")
     y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     assert B.rmsnorm_fwd_strided(xb, ld, gt, y, N, rstd, M, N, 1e-6, dtype, 0) == 0
-    o_dy = torch.full((M, ld), 1234.0, dtype=torch.bfloat16, device="cuda")
-    o_x = torch.full((M, ld), 1234.0, dtype=torch.bfloat16, device="cuda")
+    o_dy, o_x = wide(None, ld_out), wide(None, ld_out)
     o_g = torch.empty_like(gt)
     need = B.rmsnorm_bwd_bwd_workspace_size(M, N, dtype)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    assert B.rmsnorm_bwd_bwd(tb, ld, qt, dyb, ld, xb, ld, gt, rstd, o_dy, ld, o_x, ld, o_g, M, N, dtype, 0, ws,
-                             need) == 0
+    assert B.rmsnorm_bwd_bwd(tb, ld, qt, dyb, ld, xb, ld, gt, rstd, o_dy, ld_out, o_x, ld_out, o_g, M, N, dtype, 0,
+                             ws, need) == 0
     torch.cuda.synchronize()
     assert torch.all(o_dy[:, N:] == 1234.0) and torch.all(o_x[:, N:] == 1234.0)
     res = check.gate_bwd_bwd_outputs(ddx, ddg, dy, x, g, dtype, False, 1e-6,
                                      d_dy=B.to_numpy(o_dy[:, :N].contiguous(), dtype),
                                      d_x=B.to_numpy(o_x[:, :N].contiguous(), dtype), d_gamma=B.to_numpy(o_g, dtype))
-    assert gate.overall(res) == "PASS", gate.report("double backward strided", res)
+    assert gate.overall(res) == "PASS", gate.report(f"double backward strided {M}x{N} ld={ld}/{ld_out}", res)
+
+
+def test_ragged_sampled_rows_at_65536():
+    """bf16 65536x4099 on the ragged ring: d_dy and d_x gated on sampled rows,
+    d_gamma in full."""
+    M, N, dtype = 65536, 4099, "bfloat16"
+    assert _plan(M, N, dtype, aligned16=0).startswith("ragged")
+    x, g, dy = inputs.make_inputs(M, N, dtype, seed=31)
+    ddx, ddg = _cotangents(M, N, dtype, 31)
+    d_dy, d_x, d_g = gpu_util.dbwd_run(ddx, ddg, dy, x, g, dtype)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(24), np.arange(M - 24, M), rng.choice(M, 120, replace=False)]))
+    res = check.gate_bwd_bwd_outputs(ddx, ddg, dy, x, g, dtype, False, 1e-6, d_dy=d_dy[rows], d_x=d_x[rows],
+                                     rows=rows)
+    res += check.gate_bwd_bwd_outputs(ddx, ddg, dy, x, g, dtype, False, 1e-6, d_gamma=d_g)
+    assert gate.overall(res) == "PASS", gate.report("double backward bf16 65536x4099", res)
 
 
 def test_headline_shape_sampled_rows():
