@@ -22,7 +22,10 @@
  * same status and dtype codes, 1 <= N <= RMSNORM_MAX_N). Rows have explicit
  * pitches in elements (ld = N is dense). 16-byte aligned rows, pitches and
  * per-column pointers with N*sizeof(dtype) a multiple of 16 take the TMA path
- * (clusters for rows over 4096 elements); anything else the general path.
+ * (clusters for rows over 4096 elements); rows of ddx, dy and x at one 16-byte
+ * phase (equal pointer phases, pitches equal modulo 16 bytes; outputs at any
+ * phase) take the ragged TMA path up to 4100 fp32 or 7672 bf16 / fp16
+ * elements; anything else the general path.
  */
 #ifndef RMSNORM_DOUBLE_BACKWARD_H
 #define RMSNORM_DOUBLE_BACKWARD_H

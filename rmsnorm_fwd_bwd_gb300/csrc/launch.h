@@ -47,7 +47,7 @@ constexpr int kRowVecPhases = 8;
 // the row with 256 threads.
 constexpr int kTmaMaxThreads = 256;
 // The ragged double backward may take up to 10 warps: fp32 rows of up to 16 KB
-// then need at most four vectors per thread, bf16 rows of up to 7680 elements
+// then need at most four vectors per thread, 2-byte rows of up to 7672 elements
 // three.
 constexpr int kRaggedDbwdMaxThreads = 320;
 constexpr int kScalarThreads = 256;

@@ -69,6 +69,10 @@ SHAPES = [
     ("bfloat16", 20, 7001, "ragged"),
     ("bfloat16", 20, 8001, "scalar"),
     ("float32", 16, 5001, "scalar"),
+    # the ragged ring's limits: 320 threads x 3 vectors (2-byte), a 16 KB + 32 byte span (fp32)
+    ("bfloat16", 9, 7671, "ragged"),
+    ("bfloat16", 9, 7673, "scalar"),
+    ("float32", 9, 4101, "scalar"),
 ]
 
 
