@@ -393,12 +393,13 @@ bool plan_ragged(int pass, int64_t M, int N, int dt, int offset, int dev, const 
                                                            kMaxBlocksPerSm));
     } else {
         if (!bps) {
-            // the double backward holds three rows in registers and is latency-bound:
-            // as many blocks as fit (bf16 N = 4099: 2 blocks of 2 stages, 4794 GB/s
-            // at 65536 rows against 3100 with the ring rule's one; fp16 N = 1001: 10
-            // blocks, 3976 against 3057 with 4)
-            bps = pass == 4 ? kMaxBlocksPerSm
-                            : static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
+            // the ragged backwards hold their rows in registers and are latency-bound:
+            // as many blocks as fit, the ring depth shared among them (measured:
+            // double backward bf16 N = 4099 2 blocks, 4794 GB/s at 65536 rows against
+            // 3100 with one; fp32 N = 4099 backward 2 blocks, 5467 against 5160, and
+            // LayerNorm 5257 against 4424; fp16 N = 1001 backward 6 blocks, 4390
+            // against 3434 with 4)
+            bps = kMaxBlocksPerSm;
             int fit = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, k, threads, static_cast<size_t>(stage + 8 + fixed)) ==
                     cudaSuccess && fit >= 1 && fit < bps)
