@@ -274,6 +274,59 @@ bool plan_scalar(int pass, int64_t M, int N, int dt, int offset, int dev, const 
     return true;
 }
 
+// Widest aligned row (bytes) the narrow-row path takes, per pass (measured with
+// the L2 flushed between runs: at exactly 2 KB the ring path is ahead for the
+// RMSNorm forward, 6248 against 6102 GB/s for bf16 N = 1024, and the fp32
+// RMSNorm backward, 5701 against 5390; below that, and for every other
+// backward, the lanes win: bf16 N = 640 forward 5859 against 4622, bf16
+// N = 1024 backward 5390 against 4099, LayerNorm by 10-60%).
+int64_t lane_max_row_bytes(int pass, int dt) {
+    if (pass == 0 || (pass == 1 && dt == RMSNORM_F32)) return kLaneMaxRowBytes - 16;
+    return kLaneMaxRowBytes;
+}
+
+// Narrow-row path: aligned rows up to lane_max_row_bytes, a row per group of G
+// lanes (the fewest, at least 4, that hold the row at up to kv_max vectors per
+// lane: 4 for the forwards, 3 for the backwards, whose dgamma sums take
+// registers -- bf16 N = 128 backward 5489 GB/s with 8 x 2 against 5133 with
+// 4 x 4), as many blocks of kLaneThreads as fit. Overrides of threads or
+// vectors per thread send the pass to the ring path instead.
+bool plan_lanes(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
+    if (pass < 0 || pass > 3) return false;
+    const Override& ov = g_override[pass];
+    if (ov.threads || ov.vpt) return false;
+    const int64_t rowb = static_cast<int64_t>(N) * elem_bytes(dt);
+    if (rowb % 16 != 0 || rowb > lane_max_row_bytes(pass, dt)) return false;
+    const int nvec = static_cast<int>(rowb / 16);
+    const int kv_max = (pass == 0 || pass == 2) ? 4 : 3;
+    int G = 4;
+    while (G < 32 && kv_max * G < nvec) G *= 2;
+    const int kv = static_cast<int>(ceil_div(nvec, G));
+    if (kv < 1 || kv > 4) return false;
+    p.path = kPathLanes;
+    p.dtype = dt;
+    p.offset = offset;
+    p.cluster = 1;
+    p.threads = kLaneThreads;
+    p.lanes = G;
+    p.per_thread = kv;
+    p.stages = 0;
+    const int groups = kLaneThreads / G;
+    // the backwards add up their groups' sums in shared memory, a row per group
+    const int64_t sums = (pass == 1 || pass == 3) ? groups : 0;
+    p.smem = static_cast<size_t>(sums * N * 4);
+    const void* k = kernel_for(pass, p);
+    if (!k || !prepare_kernel(k, dev, di)) return false;
+    int64_t units = 0;
+    if (!occupancy_units(k, p, di, ov.blocks_per_sm, units)) return false;
+    if (sums) {
+        const int64_t cap = std::max<int64_t>(di.sms, kScalarWorkspaceCap / (4 * static_cast<int64_t>(N)));
+        if (units > cap) units = cap;
+    }
+    p.units = std::max<int64_t>(1, std::min<int64_t>(units, ceil_div(M, groups)));
+    return true;
+}
+
 // Row-vector path: rows that are not 16-byte multiples or start off a 16-byte
 // boundary, up to kRowVecMaxKv vectors per thread; as many blocks as fit.
 bool plan_rowvec(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
@@ -433,7 +486,9 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
               Plan& p) {
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
-    if (layout == kLayoutAligned && tma_shape) path = kPathTma;
+    if (layout == kLayoutAligned && tma_shape)
+        path = pass < 4 && static_cast<int64_t>(N) * elem_bytes(dt) <= lane_max_row_bytes(pass, dt) ? kPathLanes
+                                                                                                  : kPathTma;
     else if (layout != kLayoutMixed) path = kPathRowVec;
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);
@@ -442,6 +497,13 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
         return true;
     }
     bool ok = false;
+    if (path == kPathLanes) {
+        ok = plan_lanes(pass, M, N, dt, offset, dev, di, p);
+        if (!ok) {
+            (void)cudaGetLastError();
+            path = kPathTma;
+        }
+    }
     if (path == kPathTma) ok = plan_tma(pass, M, N, dt, offset, dev, di, p);
     else if (path == kPathRowVec) {
         // the ragged TMA ring first, the row-vector kernels for wider rows
@@ -907,6 +969,9 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
     if (p.path == kPathRowVec)
         snprintf(buf, buf_len, "rowvec threads=%d kv=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
                  static_cast<long long>(p.units), p.smem, di->sms);
+    else if (p.path == kPathLanes)
+        snprintf(buf, buf_len, "lanes lanes=%d kv=%d threads=%d units=%lld smem=%zu sms=%d", p.lanes, p.per_thread,
+                 p.threads, static_cast<long long>(p.units), p.smem, di->sms);
     else if (p.path == kPathRagged)
         snprintf(buf, buf_len, "ragged threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.threads,
                  p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);

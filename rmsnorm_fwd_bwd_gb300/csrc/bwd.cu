@@ -375,6 +375,7 @@ static const void* bwd_pick(const Plan& p) {
 }
 
 const void* bwd_kernel(const Plan& p) {
+    if (p.path == kPathLanes) return lanes_kernel(1, p);
     if (p.path == kPathRowVec) return rowvec_kernel(1, p);
     if (p.path == kPathRagged) return ragged_kernel(1, p);
     return p.offset ? bwd_pick<true>(p) : bwd_pick<false>(p);

@@ -263,6 +263,7 @@ static const void* fwd_pick(const Plan& p) {
 }
 
 const void* fwd_kernel(const Plan& p) {
+    if (p.path == kPathLanes) return lanes_kernel(0, p);
     if (p.path == kPathRowVec) return rowvec_kernel(0, p);
     if (p.path == kPathRagged) return ragged_kernel(0, p);
     return p.offset ? fwd_pick<true>(p) : fwd_pick<false>(p);

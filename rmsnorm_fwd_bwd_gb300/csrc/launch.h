@@ -33,7 +33,7 @@ struct RowArgs {
     uint32_t* err;         // device error word
 };
 
-enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2, kPathRagged = 3 };
+enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2, kPathRagged = 3, kPathLanes = 4 };
 
 // Most 16-byte vectors per thread on the row-vector path (256 threads).
 constexpr int kRowVecMaxKv = 5;
@@ -46,6 +46,10 @@ constexpr int kRowVecPhases = 8;
 // 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over
 // the row with 256 threads.
 constexpr int kTmaMaxThreads = 256;
+// Narrow-row path (lanes.cu): blocks of 4 warps, a row per group of 4-32 lanes,
+// aligned rows of at most kLaneMaxRowBytes.
+constexpr int kLaneThreads = 128;
+constexpr int kLaneMaxRowBytes = 2048;
 // The ragged double backward may take up to 10 warps: fp32 rows of up to 16 KB
 // then need at most four vectors per thread, 2-byte rows of up to 7672 elements
 // three.
@@ -63,6 +67,7 @@ struct Plan {
     int stages = 0;        // TMA pipeline depth
     size_t smem = 0;       // dynamic shared memory per CTA
     int64_t units = 0;     // clusters (TMA) or CTAs (scalar) = rows of dgamma partials
+    int lanes = 0;         // narrow-row path: lanes per row (per_thread: vectors per lane)
 };
 
 // Kernel entry for a plan (used for occupancy queries and attributes).
@@ -74,6 +79,7 @@ const void* ln_ragged_kernel(int pass, const Plan& p);  // the same for LayerNor
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
+const void* lanes_kernel(int pass, const Plan& p);    // narrow rows, passes 0-3
 const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA, ragged or scalar path)
 const void* dbwd_ragged_kernel_ptr(const Plan& p);    // its ragged TMA kernel
 const void* dgamma_reduce_kernel_ptr(int dtype);

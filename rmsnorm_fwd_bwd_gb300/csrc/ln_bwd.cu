@@ -317,6 +317,7 @@ static const void* ln_bwd_for(const Plan& p) {
 }
 
 const void* ln_bwd_kernel(const Plan& p) {
+    if (p.path == kPathLanes) return lanes_kernel(3, p);
     if (p.path == kPathRowVec) return ln_rowvec_kernel(3, p);
     if (p.path == kPathRagged) return ln_ragged_kernel(3, p);
     switch (p.dtype) {

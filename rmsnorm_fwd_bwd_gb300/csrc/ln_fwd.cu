@@ -300,6 +300,7 @@ static const void* ln_fwd_for(const Plan& p) {
 }
 
 const void* ln_fwd_kernel(const Plan& p) {
+    if (p.path == kPathLanes) return lanes_kernel(2, p);
     if (p.path == kPathRowVec) return ln_rowvec_kernel(2, p);
     if (p.path == kPathRagged) return ln_ragged_kernel(2, p);
     switch (p.dtype) {

@@ -54,10 +54,11 @@ def _plan(pass_, M, N, dtype, aligned16=1):
 
 # (dtype, M, N, expected path prefix of the forward plan)
 SHAPES = [
-    ("float32", 64, 256, "tma cluster=1"),
+    ("float32", 64, 256, "lanes"),
     ("bfloat16", 300, 4096, "tma cluster=1"),
-    ("float16", 129, 1000, "tma cluster=1"),
-    ("bfloat16", 77, 8, "tma cluster=1"),
+    ("float16", 129, 1000, "lanes"),
+    ("bfloat16", 77, 8, "lanes"),
+    ("bfloat16", 65, 2048, "tma cluster=1"),
     ("float32", 41, 8192, "tma cluster=2"),
     ("bfloat16", 40, 16384, "tma cluster=2"),
     ("float16", 33, 12288, "tma cluster=2"),
@@ -230,7 +231,9 @@ def test_rejections_write_nothing():
     need = B.layernorm_bwd_workspace_size(M, N, "bfloat16")
     assert need > 0
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    assert B.layernorm_bwd(x, N, x, N, g, m, r, dx, N, dg, db, M, N, "bfloat16", ws, need - 16) == 6
+    # the size query covers every layout's plan; one row of each plane of partials
+    # is less than any plan needs
+    assert B.layernorm_bwd(x, N, x, N, g, m, r, dx, N, dg, db, M, N, "bfloat16", ws, 2 * N * 4 - 16) == 6
     assert B.layernorm_bwd(x, N, x, N, g, None, r, dx, N, dg, db, M, N, "bfloat16", ws, need) == 1
     torch.cuda.synchronize()
     assert torch.all(y == 3.0) and torch.all(m == 5.0) and torch.all(r == 5.0)
