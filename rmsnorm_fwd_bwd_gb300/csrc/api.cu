@@ -292,13 +292,13 @@ int64_t lane_max_row_bytes(int pass, int dt) {
 // 4 x 4), as many blocks of kLaneThreads as fit. Overrides of threads or
 // vectors per thread send the pass to the ring path instead.
 bool plan_lanes(int pass, int64_t M, int N, int dt, int offset, int dev, const DeviceInfo& di, Plan& p) {
-    if (pass < 0 || pass > 3) return false;
+    if (pass < 0 || pass > 4) return false;
     const Override& ov = g_override[pass];
     if (ov.threads || ov.vpt) return false;
     const int64_t rowb = static_cast<int64_t>(N) * elem_bytes(dt);
     if (rowb % 16 != 0 || rowb > lane_max_row_bytes(pass, dt)) return false;
     const int nvec = static_cast<int>(rowb / 16);
-    const int kv_max = (pass == 0 || pass == 2) ? 4 : 3;
+    const int kv_max = (pass == 0 || pass == 2) ? 4 : (pass == 4 ? 2 : 3);
     int G = 4;
     while (G < 32 && kv_max * G < nvec) G *= 2;
     const int kv = static_cast<int>(ceil_div(nvec, G));
@@ -313,7 +313,7 @@ bool plan_lanes(int pass, int64_t M, int N, int dt, int offset, int dev, const D
     p.stages = 0;
     const int groups = kLaneThreads / G;
     // the backwards add up their groups' sums in shared memory, a row per group
-    const int64_t sums = (pass == 1 || pass == 3) ? groups : 0;
+    const int64_t sums = (pass == 1 || pass == 3 || pass == 4) ? groups : 0;
     p.smem = static_cast<size_t>(sums * N * 4);
     const void* k = kernel_for(pass, p);
     if (!k || !prepare_kernel(k, dev, di)) return false;
@@ -487,8 +487,7 @@ bool get_plan(int pass, int64_t M, int N, int dt, int offset, int layout, int de
     const bool tma_shape = (static_cast<int64_t>(N) * elem_bytes(dt)) % 16 == 0;
     int path = kPathScalar;
     if (layout == kLayoutAligned && tma_shape)
-        path = pass < 4 && static_cast<int64_t>(N) * elem_bytes(dt) <= lane_max_row_bytes(pass, dt) ? kPathLanes
-                                                                                                  : kPathTma;
+        path = static_cast<int64_t>(N) * elem_bytes(dt) <= lane_max_row_bytes(pass, dt) ? kPathLanes : kPathTma;
     else if (layout != kLayoutMixed) path = kPathRowVec;
     auto key = std::make_tuple(pass, dev, M, N, dt * 2 + offset, path, layout, g_override_gen);
     auto it = g_plans.find(key);

@@ -357,6 +357,7 @@ template <int DT, bool OFF>
 static const void* dbwd_for(const Plan& p) {
     if (p.path == kPathScalar) return reinterpret_cast<const void*>(&dbwd_scalar_kernel<DT, OFF>);
     if (p.path == kPathRagged) return dbwd_ragged_kernel_ptr(p);
+    if (p.path == kPathLanes) return lanes_kernel(4, p);
     if (p.path != kPathTma) return nullptr;
     return p.cluster > 1 ? dbwd_tma_vpt<DT, OFF, true>(p.per_thread) : dbwd_tma_vpt<DT, OFF, false>(p.per_thread);
 }

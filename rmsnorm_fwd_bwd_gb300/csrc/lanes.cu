@@ -1,4 +1,5 @@
-// lanes.cu -- RMSNorm and LayerNorm forward and backward for narrow rows (at most
+// lanes.cu -- RMSNorm and LayerNorm forward and backward, and the RMSNorm double
+// backward, for narrow rows (at most
 // 2 KB, 16-byte aligned): a row per group of G lanes (G = 4, 8, 16 or 32, so a
 // group never straddles a warp; the fewest that hold the row at up to three or
 // four vectors per lane), with no block barrier per row.
@@ -462,15 +463,137 @@ __global__ void __launch_bounds__(kLaneThreads) ln_bwd_lanes_kernel(const RowArg
 }
 
 // ---------------------------------------------------------------------------
+// RMSNorm double backward (formulas of dbwd.cu): per row, with u = dy * g,
+// c = mean(u * x), A = mean(ddx * x), B + D = mean(ddx * u) + mean(ddg * dy * x),
+// e = ddx - r^2 * x * A: d_dy = g * r * e + r * x * ddg,
+// d_x = r * ddg * dy - r^3 * (c * ddx + u * A + x * (B + D)) + 3 * r^5 * c * A * x,
+// d_gamma partial += r * dy * e.
+// ---------------------------------------------------------------------------
+template <int DT, int G, int KV, bool OFFSET>
+__global__ void __launch_bounds__(kLaneThreads) dbwd_lanes_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int N = a.N;
+    const int nvec = N / VEC;
+    float* red = reinterpret_cast<float*>(smem);  // [groups][N] d_gamma sums
+    const Lanes<G> L(a.M);
+    const size_t x_pitch = static_cast<size_t>(a.ldx) * E::kBytes;
+    const size_t dy_pitch = static_cast<size_t>(a.lddy) * E::kBytes;
+    const size_t t_pitch = static_cast<size_t>(a.ldddx) * E::kBytes;
+    const size_t odx_pitch = static_cast<size_t>(a.lddx) * E::kBytes;
+    const size_t ody_pitch = static_cast<size_t>(a.ldd_dy) * E::kBytes;
+    const char* xb = static_cast<const char*>(a.x);
+    const char* dyb = static_cast<const char*>(a.dy);
+    const char* tb = static_cast<const char*>(a.ddx);
+    char* odxb = static_cast<char*>(a.dx);
+    char* odyb = static_cast<char*>(a.d_dy);
+
+    griddep_wait();
+    float gw[KV][VEC], qw[KV][VEC];
+    load_cols<DT, G, KV, OFFSET>(a.gamma, nvec, L.li, gw);
+    if (a.ddg) {
+        load_cols<DT, G, KV, false>(a.ddg, nvec, L.li, qw);
+    } else {
+#pragma unroll
+        for (int k = 0; k < KV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) qw[k][e] = 0.f;
+    }
+    float acc[KV][VEC];
+#pragma unroll
+    for (int k = 0; k < KV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[k][e] = 0.f;
+
+    RowQueue<G, KV, 1> xq, dq, tq;
+    ScalarQueue<1> rq;
+    xq.fill(xb, L.gid, L.T, x_pitch, a.M, nvec, L.li);
+    dq.fill(dyb, L.gid, L.T, dy_pitch, a.M, nvec, L.li);
+    tq.fill(tb, L.gid, L.T, t_pitch, a.M, nvec, L.li);
+    rq.fill(a.rstd_in, L.gid, L.T, a.M);
+    const float inv_n = 1.0f / static_cast<float>(N);
+    for (int64_t j = 0; j < L.iters; ++j) {
+        const int64_t row = L.gid + j * L.T;
+        const int64_t ahead = row + L.T;
+        uint4 xn[KV], dn[KV], tn[KV];
+        load_row<G, KV>(xb, ahead, x_pitch, a.M, nvec, L.li, xn);
+        load_row<G, KV>(dyb, ahead, dy_pitch, a.M, nvec, L.li, dn);
+        load_row<G, KV>(tb, ahead, t_pitch, a.M, nvec, L.li, tn);
+        const float r_nxt = ahead < a.M ? __ldg(a.rstd_in + ahead) : 0.f;
+        const float r = rq.q[0];
+        float pc = 0.f, pa = 0.f, pb = 0.f, pd = 0.f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            if (L.li + k * G < nvec) {
+                float xf[VEC], df[VEC], tf[VEC];
+                E::unpack(xq.q[0][k], xf);
+                E::unpack(dq.q[0][k], df);
+                E::unpack(tq.q[0][k], tf);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float u = __fmul_rn(df[e], gw[k][e]);
+                    pc = fmaf(u, xf[e], pc);
+                    pa = fmaf(tf[e], xf[e], pa);
+                    pb = fmaf(tf[e], u, pb);
+                    pd = fmaf(__fmul_rn(qw[k][e], df[e]), xf[e], pd);
+                }
+            }
+        }
+        const float c = group_allsum<G>(pc) * inv_n;
+        const float A = group_allsum<G>(pa) * inv_n;
+        const float bd = (group_allsum<G>(pb) + group_allsum<G>(pd)) * inv_n;  // B + D
+        const float r2 = r * r;
+        const float r3 = r2 * r;
+        const float r2a = r2 * A;
+        const float k5 = (3.0f * (r3 * r2)) * (c * A);
+        if (row < a.M) {
+            char* odx_row = odxb + static_cast<size_t>(row) * odx_pitch;
+            char* ody_row = odyb + static_cast<size_t>(row) * ody_pitch;
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int idx = L.li + k * G;
+                if (idx < nvec) {
+                    float xf[VEC], df[VEC], tf[VEC], o_dy[VEC], o_x[VEC];
+                    E::unpack(xq.q[0][k], xf);
+                    E::unpack(dq.q[0][k], df);
+                    E::unpack(tq.q[0][k], tf);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float x = xf[e], d = df[e], t = tf[e], g = gw[k][e], q = qw[k][e];
+                        const float u = __fmul_rn(d, g);
+                        const float ee = fmaf(-r2a, x, t);  // ddx - r^2 x A
+                        o_dy[e] = fmaf(g * r, ee, (r * x) * q);
+                        const float inner = fmaf(x, bd, fmaf(c, t, u * A));
+                        o_x[e] = fmaf(k5, x, fmaf(-r3, inner, (r * q) * d));
+                        acc[k][e] = fmaf(r * d, ee, acc[k][e]);
+                    }
+                    stg128(ody_row + idx * 16, E::pack(o_dy));
+                    stg128(odx_row + idx * 16, E::pack(o_x));
+                }
+            }
+        }
+        xq.push(xn);
+        dq.push(dn);
+        tq.push(tn);
+        rq.push(r_nxt);
+    }
+    griddep_launch_dependents();
+    block_partials<G, KV, VEC>(acc, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * N);
+}
+
+// ---------------------------------------------------------------------------
 // dispatch: G lanes x KV vectors, the fewest lanes (at least 4) that hold the
 // row at up to kv_max vectors each: kv_max = 4 for the forwards, 3 for the
-// backwards (their sums take registers), except rows of 128 vectors (G = 32, KV
-// = 4). Only those instances exist.
+// backwards (their sums take registers), 2 for the double backward (three rows
+// and two per-column vectors in registers), except where 32 lanes need more.
+// Only those instances exist.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr bool lanes_instance(int pass, int G, int KV) {
     if (pass == 0 || pass == 2) return G == 4 ? KV >= 1 && KV <= 4 : KV == 3 || KV == 4;
+    if (pass == 4) return G == 4 ? KV == 1 || KV == 2 : (KV == 2 || (G == 32 && (KV == 3 || KV == 4)));
     return G == 4 ? KV >= 1 && KV <= 3 : (KV == 2 || KV == 3 || (G == 32 && KV == 4));
 }
 
@@ -493,6 +616,11 @@ const void* lanes_entry(int pass, bool offset) {
         return nullptr;
     case 3:
         if constexpr (lanes_instance(3, G, KV)) return reinterpret_cast<const void*>(&ln_bwd_lanes_kernel<DT, G, KV>);
+        return nullptr;
+    case 4:
+        if constexpr (lanes_instance(4, G, KV))
+            return offset ? reinterpret_cast<const void*>(&dbwd_lanes_kernel<DT, G, KV, true>)
+                          : reinterpret_cast<const void*>(&dbwd_lanes_kernel<DT, G, KV, false>);
         return nullptr;
     default: return nullptr;
     }

@@ -79,7 +79,7 @@ const void* ln_ragged_kernel(int pass, const Plan& p);  // the same for LayerNor
 const void* ln_fwd_kernel(const Plan& p);             // LayerNorm (TMA or scalar path)
 const void* ln_bwd_kernel(const Plan& p);
 const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 backward
-const void* lanes_kernel(int pass, const Plan& p);    // narrow rows, passes 0-3
+const void* lanes_kernel(int pass, const Plan& p);    // narrow rows, passes 0-4
 const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA, ragged or scalar path)
 const void* dbwd_ragged_kernel_ptr(const Plan& p);    // its ragged TMA kernel
 const void* dgamma_reduce_kernel_ptr(int dtype);

@@ -2,12 +2,12 @@
 oracle, and second-order autograd through rms_norm.
 
 Every case gates d_dy, d_x and d_gamma with the golden / reference / target
-gate. Shapes cover the TMA path, the cluster path (rows over 4096 elements),
-the ragged TMA path (rows off 16 bytes: odd row lengths, shifted pointers,
-odd pitches, outputs at another phase), the general path (inputs at different
-phases, rows too wide for the ragged ring), the offset variant, an absent
-ddgamma, empty inputs, strided rows and the headline shape at full size on
-sampled rows.
+gate. Shapes cover the narrow-row path (rows of at most 2 KB), the TMA path,
+the cluster path (rows over 4096 elements), the ragged TMA path (rows off 16
+bytes: odd row lengths, shifted pointers, odd pitches, outputs at another
+phase), the general path (inputs at different phases, rows too wide for the
+ragged ring), the offset variant, an absent ddgamma, empty inputs, strided rows
+and the headline shape at full size on sampled rows.
 """
 import numpy as np
 import pytest
@@ -54,10 +54,16 @@ def _plan(M, N, dtype, aligned16=1):
 
 
 SHAPES = [
-    ("float32", 64, 256, "tma cluster=1"),
+    # narrow rows (at most 2 KB): a row per group of lanes, every (lanes, vectors) instance
+    ("bfloat16", 77, 8, "lanes lanes=4 kv=1 "),
+    ("bfloat16", 65, 64, "lanes lanes=4 kv=2 "),
+    ("bfloat16", 300, 128, "lanes lanes=8 kv=2 "),
+    ("float32", 64, 256, "lanes lanes=32 kv=2 "),
+    ("bfloat16", 99, 256, "lanes lanes=16 kv=2 "),
+    ("bfloat16", 130, 768, "lanes lanes=32 kv=3 "),
+    ("float16", 129, 1000, "lanes lanes=32 kv=4 "),
+    ("bfloat16", 300, 2048, "tma cluster=1"),
     ("bfloat16", 300, 4096, "tma cluster=1"),
-    ("float16", 129, 1000, "tma cluster=1"),
-    ("bfloat16", 77, 8, "tma cluster=1"),
     ("float32", 41, 8192, "tma cluster=2"),
     ("bfloat16", 40, 16384, "tma cluster=4"),
     ("float32", 24, 16384, "tma cluster=4"),
@@ -84,8 +90,9 @@ def test_shapes_and_paths(dtype, M, N, path, offset):
 
 
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
-def test_without_ddgamma(dtype):
-    _gate(96, 2048, dtype, seed=5, with_ddg=False, title=f"double backward {dtype} ddgamma absent")
+@pytest.mark.parametrize("N", [256, 2048])
+def test_without_ddgamma(dtype, N):
+    _gate(96, N, dtype, seed=5, with_ddg=False, title=f"double backward {dtype} N={N} ddgamma absent")
 
 
 @pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
