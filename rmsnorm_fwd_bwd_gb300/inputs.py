@@ -82,6 +82,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("ln_bf16_65536x4096", 65536, 4096, "bfloat16", eps=1e-5, op="layernorm", row_shift=2.0),
     Workload("ln_fp32_16384x16384", 16384, 16384, "float32", eps=1e-5, op="layernorm", row_shift=2.0),
     Workload("ln_bf16_16384x4099", 16384, 4099, "bfloat16", eps=1e-5, op="layernorm", row_shift=2.0),
+    # narrow rows (a row per group of lanes)
+    Workload("bf16_1048576x128", 1 << 20, 128, "bfloat16"),
+    Workload("ln_bf16_524288x256", 524288, 256, "bfloat16", eps=1e-5, op="layernorm", row_shift=2.0),
 ]}
 
 HEADLINE = "bf16_65536x4096"
