@@ -27,8 +27,13 @@
 
 namespace rmsnorm {
 
+// Minimum resident 256-thread blocks for __launch_bounds__ (0: none). The
+// 64-element instances (2-byte types, 8 vectors per thread: the split-row plans,
+// 128-thread blocks) are held to 128 registers, four blocks per SM.
+template <int DT, int VPT> struct FwdTmaMinBlocks { static constexpr int value = Elem<DT>::kVec * VPT >= 64 ? 2 : 0; };
+
 template <int DT, int VPT, bool OFFSET, bool CLUSTER>
-__global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::value)) fwd_tma_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -67,18 +72,28 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
     }
     griddep_wait();  // inputs may come from the previous kernel on the stream
 
-    // gamma slice widened to fp32 once (offset variant: 1 + w), kept in registers
-    float gf[VPT][VEC];
+    // gamma slice widened to fp32 once (offset variant: 1 + w), kept in registers;
+    // at 64 elements per thread (2-byte types, 8 vectors) x and gamma stay as raw
+    // 16-byte words instead and are widened where used, which halves their
+    // registers and lets more blocks share an SM
+    constexpr bool PACK = VEC * VPT >= 64;
+    float gf[PACK ? 1 : VPT][VEC];
+    uint4 gr[PACK ? VPT : 1];
     {
         const uint4* gs = reinterpret_cast<const uint4*>(
             static_cast<const char*>(a.gamma) + static_cast<size_t>(crank) * slice_bytes);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
-            E::unpack(idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0), gf[v]);
-            if (OFFSET) {
+            const uint4 raw = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+            if constexpr (PACK) {
+                gr[v] = raw;
+            } else {
+                E::unpack(raw, gf[v]);
+                if (OFFSET) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) gf[v][e] = 1.0f + gf[v][e];
+                    for (int e = 0; e < VEC; ++e) gf[v][e] = 1.0f + gf[v][e];
+                }
             }
         }
     }
@@ -107,18 +122,21 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
 
         if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        // x slice widened to fp32 once; sum of squares on the way
-        float xf[VPT][VEC];
+        // x slice widened to fp32 once (or kept raw, see PACK); sum of squares on the way
+        float xf[PACK ? 1 : VPT][VEC];
+        uint4 xr[PACK ? VPT : 1];
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
-            E::unpack(idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0),
-                      xf[v]);
+            const uint4 raw = idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0);
+            float* xv = xf[PACK ? 0 : v];
+            if constexpr (PACK) xr[v] = raw;
+            E::unpack(raw, *reinterpret_cast<float(*)[VEC]>(xv));
 #pragma unroll
             for (int e = 0; e < VEC; e += 2) {
-                ss0 = fmaf(xf[v][e], xf[v][e], ss0);
-                ss1 = fmaf(xf[v][e + 1], xf[v][e + 1], ss1);
+                ss0 = fmaf(xv[e], xv[e], ss0);
+                ss1 = fmaf(xv[e + 1], xv[e + 1], ss1);
             }
         }
         float* redb = red + (j & 1) * 32;
@@ -160,9 +178,27 @@ __global__ void __launch_bounds__(kTmaMaxThreads) fwd_tma_kernel(const RowArgs a
                 const int idx = v * nt + tid;
                 if (idx < nvec) {
                     float o[VEC];
+                    if constexpr (PACK) {
+                        float xv[VEC], gv[VEC];
+                        // empty asm statements mark the raw words as changed, so the
+                        // compiler neither hoists gamma's widening out of the row
+                        // loop nor keeps x's widened values from the sum of squares
+                        // live across the barrier (64 registers each)
+                        uint4 gw = gr[v], xw = xr[v];
+                        asm volatile("" : "+r"(gw.x), "+r"(gw.y), "+r"(gw.z), "+r"(gw.w));
+                        asm volatile("" : "+r"(xw.x), "+r"(xw.y), "+r"(xw.z), "+r"(xw.w));
+                        E::unpack(xw, xv);
+                        E::unpack(gw, gv);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e)
-                        o[e] = OFFSET ? (gf[v][e] * xf[v][e]) * r : (xf[v][e] * r) * gf[v][e];
+                        for (int e = 0; e < VEC; ++e) {
+                            const float g = OFFSET ? 1.0f + gv[e] : gv[e];
+                            o[e] = OFFSET ? (g * xv[e]) * r : (xv[e] * r) * g;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            o[e] = OFFSET ? (gf[v][e] * xf[v][e]) * r : (xf[v][e] * r) * gf[v][e];
+                    }
                     stg128(yrow + idx * 16, E::pack(o));
                 }
             }
