@@ -54,6 +54,9 @@ METRIC = "RMSNorm fwd/bwd HBM GB/s & % of peak, bf16 M=65536 N=4096, 1 GB300"
 def metric_for(w) -> str:
     if w.op == "layernorm":
         return f"LayerNorm fwd/bwd HBM GB/s & % of peak, {w.dtype} M={w.M} N={w.N}, 1 GB300"
+    from rmsnorm_fwd_bwd_gb300 import inputs
+    if w.name != inputs.HEADLINE:
+        return f"RMSNorm fwd/bwd HBM GB/s & % of peak, {w.dtype} M={w.M} N={w.N}, 1 GB300"
     return METRIC
 
 
