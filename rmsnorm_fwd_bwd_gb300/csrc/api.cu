@@ -233,9 +233,6 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     } else {
         if (!bps) {
             bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
-            // few rows per SM: at least three blocks for the ramp (bf16 8192x5120
-            // backward 49.0 -> 44.2 us)
-            if (M <= 64 * static_cast<int64_t>(di.sms) && bps < 3) bps = 3;
             // blocks that fit by registers alone: the ring depth is sized for those
             int fit = 0;
             p.smem = static_cast<size_t>(stage + 8) + fixed;

@@ -76,6 +76,20 @@ __global__ void __launch_bounds__(kTmaMaxThreads) dbwd_tma_kernel(const RowArgs 
         fence_mbar_init();
     }
     griddep_wait();  // inputs may come from the previous kernel on the stream
+    // the first rows' copies go out before the per-column set-up below, so the
+    // ring fills while gamma is being loaded
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
+        const size_t r = static_cast<size_t>(cid + j * ncl);
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_g2s(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol);
+        bulk_g2s(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol);
+        bulk_g2s(smem_u32(st + 2 * slice_bytes), tsl + r * t_pitch, slice_bytes, bar, pol);
+    };
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stage_bytes, smem_u32(&full[j]));
+    }
 
     // g (or 1 + w) and ddg slices widened once into shared memory as VEC/4 planes of float4
     float4* gsm4 = reinterpret_cast<float4*>(gsm);
@@ -105,19 +119,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads) dbwd_tma_kernel(const RowArgs 
 
     __syncthreads();
     if (CLUSTER) cluster_sync();
-
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
-        const size_t r = static_cast<size_t>(cid + j * ncl);
-        mbar_arrive_expect_tx(bar, stage_bytes);
-        bulk_g2s(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + 2 * slice_bytes), tsl + r * t_pitch, slice_bytes, bar, pol);
-    };
-    if (tid == 0) {
-        const int64_t pre = nrows < S ? nrows : S;
-        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stage_bytes, smem_u32(&full[j]));
-    }
 
     // saved r, 32 rows per warp-wide load, fetched 32 rows ahead of use
     auto rstd_at = [&](int64_t jj) -> float { return jj < nrows ? __ldg(a.rstd_in + cid + jj * ncl) : 0.f; };

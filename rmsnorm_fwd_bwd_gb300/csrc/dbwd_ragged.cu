@@ -64,6 +64,20 @@ __global__ void __launch_bounds__(kRaggedDbwdMaxThreads) dbwd_ragged_kernel(cons
         fence_mbar_init();
     }
     griddep_wait();
+    // the first rows' copies go out before the per-column set-up below, so the
+    // ring fills while gamma is being loaded
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
+        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
+        mbar_arrive_expect_tx(bar, 3 * span);
+        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
+        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
+        bulk_g2s(smem_u32(st + 2 * stride), tb + row * t_pitch - o, span, bar, pol);
+    };
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * 3 * stride, smem_u32(&full[j]));
+    }
 
     for (int idx = tid; idx < nslot; idx += nt) {
         int c0;
@@ -93,18 +107,6 @@ __global__ void __launch_bounds__(kRaggedDbwdMaxThreads) dbwd_ragged_kernel(cons
     }
     __syncthreads();
 
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
-        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
-        mbar_arrive_expect_tx(bar, 3 * span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + 2 * stride), tb + row * t_pitch - o, span, bar, pol);
-    };
-    if (tid == 0) {
-        const int64_t pre = nrows < S ? nrows : S;
-        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * 3 * stride, smem_u32(&full[j]));
-    }
     auto rstd_at = [&](int64_t jj) -> float {
         return jj < nrows ? __ldg(a.rstd_in + blockIdx.x + jj * static_cast<int64_t>(gridDim.x)) : 0.f;
     };

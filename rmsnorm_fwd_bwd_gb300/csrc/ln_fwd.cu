@@ -73,6 +73,18 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
         fence_mbar_init();
     }
     griddep_wait();  // inputs may come from the previous kernel on the stream
+    // the first rows' copies go out before the per-column set-up below, so the
+    // ring fills while gamma is being loaded
+    const uint64_t pol = l2_evict_first_policy();
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) {
+            const uint32_t bar = smem_u32(&full[j]);
+            mbar_arrive_expect_tx(bar, slice_bytes);
+            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
+                     slice_bytes, bar, pol);
+        }
+    }
 
     // gamma and beta slices widened to fp32 once, kept in registers
     float gf[VPT][VEC], bf[VPT][VEC];
@@ -94,17 +106,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
 
     __syncthreads();
     if (CLUSTER) cluster_sync();  // peers' shared memory is live before any DSMEM read
-
-    const uint64_t pol = l2_evict_first_policy();
-    if (tid == 0) {
-        const int64_t pre = nrows < S ? nrows : S;
-        for (int64_t j = 0; j < pre; ++j) {
-            const uint32_t bar = smem_u32(&full[j]);
-            mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
-                     slice_bytes, bar, pol);
-        }
-    }
 
     bool aborted = false;
     int64_t abort_row = nrows;

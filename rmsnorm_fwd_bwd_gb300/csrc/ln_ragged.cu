@@ -76,6 +76,18 @@ __global__ void __launch_bounds__(kTmaMaxThreads, 3) ln_fwd_ragged_kernel(const 
         fence_mbar_init();
     }
     griddep_wait();
+    // the first rows' copies go out before the per-column set-up below, so the
+    // ring fills while gamma is being loaded
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
+        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
+        mbar_arrive_expect_tx(bar, span);
+        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
+    };
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stride, smem_u32(&full[j]));
+    }
     stage_slots<DT>(a.gamma, N, o, nv, nslot, gsm4);
     stage_slots<DT>(a.beta, N, o, nv, nslot, bsm4);
     unsigned bits[VPT];
@@ -88,17 +100,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads, 3) ln_fwd_ragged_kernel(const 
     }
     const float n_warp = warp_allsum(static_cast<float>(cnt));
     __syncthreads();
-
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
-        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
-        mbar_arrive_expect_tx(bar, span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
-    };
-    if (tid == 0) {
-        const int64_t pre = nrows < S ? nrows : S;
-        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * stride, smem_u32(&full[j]));
-    }
 
     bool aborted = false;
     int64_t abort_row = nrows;
@@ -241,6 +242,19 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
         fence_mbar_init();
     }
     griddep_wait();
+    // the first rows' copies go out before the per-column set-up below, so the
+    // ring fills while gamma is being loaded
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
+        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
+        mbar_arrive_expect_tx(bar, 2 * span);
+        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
+        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
+    };
+    if (tid == 0) {
+        const int64_t pre = nrows < S ? nrows : S;
+        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * 2 * stride, smem_u32(&full[j]));
+    }
     stage_slots<DT>(a.gamma, N, o, nv, nslot, gsm4);
     unsigned bits[VPT];
     float accg[VPT][VEC], accb[VPT][VEC];
@@ -253,17 +267,6 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
     }
     __syncthreads();
 
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
-        const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
-        mbar_arrive_expect_tx(bar, 2 * span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
-    };
-    if (tid == 0) {
-        const int64_t pre = nrows < S ? nrows : S;
-        for (int64_t j = 0; j < pre; ++j) issue(j, ring + j * 2 * stride, smem_u32(&full[j]));
-    }
     auto saved_at = [&](const float* p, int64_t jj) -> float {
         return jj < nrows ? __ldg(p + blockIdx.x + jj * static_cast<int64_t>(gridDim.x)) : 0.f;
     };
