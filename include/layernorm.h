@@ -33,8 +33,11 @@
  * Layout: row-major with explicit row pitches in elements (ld >= N; ld = N is
  * dense). Rows whose pitches and pointers are 16-byte aligned and whose byte
  * length is a multiple of 16 take the TMA bulk-copy path (clusters of 2 or 4
- * CTAs for rows wider than 16 KB); anything else takes a general path with
- * scalar loads. Outputs must not overlap inputs.
+ * CTAs for rows wider than 16 KB; rows of at most 2 KB a row per group of 4-32
+ * lanes instead); rows whose x and dy share their offset from a 16-byte
+ * boundary take a ragged TMA path (spans up to 16 KB) or a row-vector path
+ * (16-20 KB); anything else takes a general path with scalar loads. Outputs
+ * must not overlap inputs.
  */
 #ifndef LAYERNORM_H
 #define LAYERNORM_H

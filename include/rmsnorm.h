@@ -31,10 +31,12 @@
  *     inputs.
  *   - Pointers must be aligned to their element size. Rows whose byte length is
  *     a multiple of 16 with 16-byte-aligned x/y/dy/dx/gamma take the TMA bulk-copy
- *     path; other rows of up to ~20 KB take a path with 16-byte loads of each
- *     row's aligned span (when x and dy share their offset from a 16-byte
- *     boundary); anything else takes a general path with scalar loads. All give
- *     results within the same correctness gate.
+ *     path (rows of at most 2 KB: a row per group of 4-32 lanes with 16-byte
+ *     loads instead). When x and dy share their offset from a 16-byte boundary,
+ *     other rows of up to 16 KB take a TMA path that copies each row's aligned
+ *     span and masks its two end vectors, and rows of 16-20 KB a path with
+ *     16-byte loads of that span; anything else takes a general path with
+ *     scalar loads. All give results within the same correctness gate.
  *   - All calls are asynchronous on `stream` (NULL = legacy default stream).
  *     Validation happens on the host before any launch; when a call returns an
  *     error nothing was launched and no output was written. There is no
@@ -148,9 +150,11 @@ rmsnorm_status rmsnorm_bwd_static_scratch(const void* dy, const void* x, const v
  * rows are ld* elements apart (ld* >= N; the gaps between rows are neither read
  * nor written), e.g. a view of the first N columns of a wider matrix. With
  * ld* = N they are rmsnorm_fwd / rmsnorm_bwd. The fast paths need every row to
- * start on the same 16-byte boundary pattern: 16-byte aligned rows take the TMA
- * path; x and dy rows at equal offsets from a 16-byte boundary the row-vector
- * path; other combinations the general path. The workspace of
+ * start on the same 16-byte boundary pattern: 16-byte aligned rows and pitches
+ * take the TMA (or, up to 2 KB, the lane-group) path; x and dy rows at equal
+ * offsets from a 16-byte boundary (equal pointer offsets, pitches equal modulo
+ * 16 bytes) the ragged TMA or row-vector path; other combinations the general
+ * path. The workspace of
  * rmsnorm_bwd_strided is sized by rmsnorm_bwd_workspace_size(M, N, dtype).
  * Extension of the pages' contract, which rejects non-contiguous inputs
  * ("Check an AI model calculation before accelerating it", section "Adapting
@@ -186,13 +190,13 @@ rmsnorm_status rmsnorm_device_error(uint32_t* flags, int clear);
 rmsnorm_status rmsnorm_selftest_wait_timeout(uint32_t polls, rmsnorm_stream_t stream);
 
 /*
- * Launch plan the library would use, as text (for logs and tests), e.g.
+ * Launch plan the library would use, as text (for logs and tests): the path
+ * ("tma", "lanes", "ragged", "rowvec" or "scalar") and its shape, e.g.
  * "tma cluster=1 threads=256 vpt=2 stages=2 units=456 ...". pass: 0 = forward,
  * 1 = backward; 2 and 3: the LayerNorm forward and backward of layernorm.h; 4:
- * the double backward of rmsnorm_double_backward.h (for 4, any aligned16 other
- * than 1 means the general path). aligned16: 1 if the data pointers will be 16-byte aligned, 0 if
- * not (x and dy sharing their offset from a 16-byte boundary), 2 if x and dy
- * sit at different offsets.
+ * the double backward of rmsnorm_double_backward.h. aligned16: 1 if the data
+ * pointers will be 16-byte aligned, 0 if not (x and dy -- and ddx -- sharing
+ * their offset from a 16-byte boundary), 2 if they sit at different offsets.
  * Writes at most buf_len bytes including the terminating NUL. Host-only.
  */
 rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,
