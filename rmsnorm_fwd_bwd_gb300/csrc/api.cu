@@ -173,13 +173,17 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     const int s = elem_bytes(dt);
     const int vec = 16 / s;
     if ((static_cast<int64_t>(N) * s) % 16 != 0) return false;
-    // the double backward also splits rows so that a CTA's slice fits its register budget
+    // the double backward also splits rows so that a CTA's slice fits its register
+    // budget; unsplit, it may take up to kDbwdMaxThreads threads at two vectors each
     const int64_t max_cta_elems =
         pass == 4 ? static_cast<int64_t>(kMaxElemsPerThread[pass]) * kTmaMaxThreads : int64_t(1) << 30;
+    const int64_t max_cta_elems_unsplit =
+        pass == 4 ? static_cast<int64_t>(kMaxElemsPerThread[pass]) * kDbwdMaxThreads : max_cta_elems;
     int cl = 1;
     while (cl <= 4 && !((static_cast<int64_t>(N) * s) / cl <= kSliceMaxBytes && N % (cl * vec) == 0 &&
-                        N / cl <= max_cta_elems))
+                        N / cl <= (cl == 1 ? max_cta_elems_unsplit : max_cta_elems)))
         cl *= 2;
+    const int tmax = (pass == 4 && cl == 1) ? kDbwdMaxThreads : kTmaMaxThreads;
     if (cl > 4) return false;
     const int nvec = N / (cl * vec);
     const Override& ov = g_override[pass];
@@ -191,14 +195,17 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
         if (vpt > 8) return false;
         if (dir == 1 && (cl == 1 || pass == 4))
             while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread[pass] &&
-                   round_up(ceil_div(nvec, vpt / 2), 32) <= kTmaMaxThreads)
+                   round_up(ceil_div(nvec, vpt / 2), 32) <= tmax)
                 vpt /= 2;  // more threads rather than more registers
         while (vpt > 1 && ceil_div(nvec, vpt / 2) <= 32) vpt /= 2;  // tiny rows: one warp
     }
     if (vpt != 1 && vpt != 2 && vpt != 4 && vpt != 8) return false;
     int threads = ov.threads ? ov.threads : static_cast<int>(round_up(ceil_div(nvec, vpt), 32));
     if (threads < 32) threads = 32;
-    if (threads % 32 != 0 || threads > kTmaMaxThreads) return false;
+    // block-size bound of the kernel instance (the double backward's unsplit
+    // instances of up to two vectors per thread take up to kDbwdMaxThreads)
+    const int tbound = (pass == 4 && cl == 1 && vpt <= 2) ? kDbwdMaxThreads : kTmaMaxThreads;
+    if (threads % 32 != 0 || threads > tbound) return false;
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
     if (cl > 8) return false;
     const int slice = (N / cl) * s;

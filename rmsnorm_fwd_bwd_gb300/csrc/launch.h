@@ -46,6 +46,9 @@ constexpr int kRowVecPhases = 8;
 // 1024 16-byte vectors, i.e. 256 threads x 4 vectors; the scalar path loops over
 // the row with 256 threads.
 constexpr int kTmaMaxThreads = 256;
+// The double backward's single-CTA plans may take up to 16 warps (rows of up to
+// 8192 elements at two vectors per thread, without a cluster barrier per row).
+constexpr int kDbwdMaxThreads = 512;
 // Narrow-row path (lanes.cu): blocks of 4 warps, a row per group of 4-32 lanes,
 // aligned rows of at most kLaneMaxRowBytes.
 constexpr int kLaneThreads = 128;
