@@ -179,11 +179,16 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
         pass == 4 ? static_cast<int64_t>(kMaxElemsPerThread[pass]) * kTmaMaxThreads : int64_t(1) << 30;
     const int64_t max_cta_elems_unsplit =
         pass == 4 ? static_cast<int64_t>(kMaxElemsPerThread[pass]) * kDbwdMaxThreads : max_cta_elems;
+    // the RMSNorm backward keeps rows of up to kWideRowMaxBytes in one block of up
+    // to kWideRowThreads threads
+    const int64_t max_slice_unsplit = pass == 1 ? kWideRowMaxBytes : kSliceMaxBytes;
     int cl = 1;
-    while (cl <= 4 && !((static_cast<int64_t>(N) * s) / cl <= kSliceMaxBytes && N % (cl * vec) == 0 &&
-                        N / cl <= (cl == 1 ? max_cta_elems_unsplit : max_cta_elems)))
+    while (cl <= 4 &&
+           !((static_cast<int64_t>(N) * s) / cl <= (cl == 1 ? max_slice_unsplit : kSliceMaxBytes) &&
+             N % (cl * vec) == 0 && N / cl <= (cl == 1 ? max_cta_elems_unsplit : max_cta_elems)))
         cl *= 2;
-    const int tmax = (pass == 4 && cl == 1) ? kDbwdMaxThreads : kTmaMaxThreads;
+    const int tmax = cl == 1 ? (pass == 4 ? kDbwdMaxThreads : (pass == 1 ? kWideRowThreads : kTmaMaxThreads))
+                             : kTmaMaxThreads;
     if (cl > 4) return false;
     const int nvec = N / (cl * vec);
     const Override& ov = g_override[pass];
@@ -192,6 +197,9 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
         const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kThreadCap[pass]);
         for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
+        // rows wider than the thread cap holds at 8 vectors (the RMSNorm
+        // backward's 16-32 KB rows): four vectors per thread on up to tmax threads
+        if (vpt > 8 && !ov.threads && round_up(ceil_div(nvec, 4), 32) <= tmax) vpt = 4;
         if (vpt > 8) return false;
         if (dir == 1 && (cl == 1 || pass == 4))
             while (vpt > kMinVpt && vpt * vec > kMaxElemsPerThread[pass] &&
@@ -204,7 +212,9 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     if (threads < 32) threads = 32;
     // block-size bound of the kernel instance (the double backward's unsplit
     // instances of up to two vectors per thread take up to kDbwdMaxThreads)
-    const int tbound = (pass == 4 && cl == 1 && vpt <= 2) ? kDbwdMaxThreads : kTmaMaxThreads;
+    const int tbound = (pass == 4 && cl == 1 && vpt <= 2)   ? kDbwdMaxThreads
+                       : (pass == 1 && cl == 1 && vpt <= 4) ? kWideRowThreads
+                                                            : kTmaMaxThreads;
     if (threads % 32 != 0 || threads > tbound) return false;
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
     if (cl > 8) return false;

@@ -26,9 +26,19 @@ namespace rmsnorm {
 // floor of 2 blocks (at most 128 registers) gives it 96 and no spills.
 template <int DT, int VPT> struct BwdMinBlocks { static constexpr int value = 0; };
 template <> struct BwdMinBlocks<kF32, 4> { static constexpr int value = 2; };
+// Block-size bound: the unsplit instances of up to four vectors per thread may
+// take kWideRowThreads threads (one block per row of up to 32 KB instead of a
+// two-CTA cluster); their register cap is then 128, as the floor above gives the
+// fp32 4-vector instance.
+template <int DT, int VPT, bool CLUSTER> struct BwdTmaBounds {
+    static constexpr bool wide = !CLUSTER && VPT <= 4;
+    static constexpr int threads = wide ? kWideRowThreads : kTmaMaxThreads;
+    static constexpr int min_blocks = wide ? (BwdMinBlocks<DT, VPT>::value ? 1 : 0) : BwdMinBlocks<DT, VPT>::value;
+};
 
 template <int DT, int VPT, bool OFFSET, bool CLUSTER>
-__global__ void __launch_bounds__(kTmaMaxThreads, (BwdMinBlocks<DT, VPT>::value)) bwd_tma_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(BwdTmaBounds<DT, VPT, CLUSTER>::threads, (BwdTmaBounds<DT, VPT, CLUSTER>::min_blocks))
+    bwd_tma_kernel(const RowArgs a) {
     using E = Elem<DT>;
     constexpr int VEC = E::kVec;
     extern __shared__ __align__(128) unsigned char smem[];

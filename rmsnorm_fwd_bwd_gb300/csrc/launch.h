@@ -49,6 +49,10 @@ constexpr int kTmaMaxThreads = 256;
 // The double backward's single-CTA plans may take up to 16 warps (rows of up to
 // 8192 elements at two vectors per thread, without a cluster barrier per row).
 constexpr int kDbwdMaxThreads = 512;
+// The RMSNorm backward's single-CTA plans for rows of 16-32 KB: 16 warps at up to
+// four vectors per thread, instead of a two-CTA cluster.
+constexpr int kWideRowThreads = 512;
+constexpr int kWideRowMaxBytes = 32768;
 // Narrow-row path (lanes.cu): blocks of 4 warps, a row per group of 4-32 lanes,
 // aligned rows of at most kLaneMaxRowBytes.
 constexpr int kLaneThreads = 128;

@@ -79,7 +79,9 @@ SHAPES = [((3, 255), "float32"), ((3, 256), "bfloat16"), ((3, 257), "bfloat16"),
           ((8, 4096), "bfloat16"), ((8, 4097), "bfloat16"), ((8, 5120), "bfloat16"),
           # rows off 16 bytes: the ragged TMA ring (bf16, fp16 and fp32 up to 16 KB)
           # and the row-vector kernels (rows of 16-20 KB)
-          ((29, 4099), "float32"), ((31, 4097), "float16"), ((33, 9999), "bfloat16")]
+          ((29, 4099), "float32"), ((31, 4097), "float16"), ((33, 9999), "bfloat16"),
+          # 16-32 KB rows: the backward's one-block (up to 512 threads) plans
+          ((5, 16384), "float16"), ((7, 8192), "float32"), ((3, 10240), "bfloat16")]
 
 
 @pytest.mark.parametrize("shape,dtype", SHAPES)
@@ -243,7 +245,12 @@ def test_plan_dispatch():
     assert B.rmsnorm_describe_plan(0, 65536, 4096, "bfloat16").startswith("tma cluster=1")
     assert B.rmsnorm_describe_plan(1, 65536, 4096, "bfloat16").startswith("tma cluster=1")
     assert B.rmsnorm_describe_plan(0, 16384, 16384, "float32").startswith("tma cluster=4")
-    assert B.rmsnorm_describe_plan(1, 16384, 16384, "float16").startswith("tma cluster=2")
+    # 32 KB rows: the forward splits them over a cluster, the backward keeps them
+    # in one 512-thread block
+    assert B.rmsnorm_describe_plan(0, 16384, 16384, "float16").startswith("tma cluster=2")
+    assert B.rmsnorm_describe_plan(1, 16384, 16384, "float16").startswith("tma cluster=1 threads=512 vpt=4")
+    assert B.rmsnorm_describe_plan(1, 16384, 8192, "float32").startswith("tma cluster=1 threads=512 vpt=4")
+    assert B.rmsnorm_describe_plan(1, 16384, 16384, "float32").startswith("tma cluster=4")
     assert B.rmsnorm_describe_plan(0, 8192, 4099, "bfloat16").startswith("ragged")
     assert B.rmsnorm_describe_plan(1, 8192, 4099, "bfloat16").startswith("ragged")
     assert B.rmsnorm_describe_plan(0, 8192, 4096, "bfloat16", aligned16=False).startswith("ragged")
