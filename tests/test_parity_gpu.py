@@ -245,9 +245,8 @@ def test_plan_dispatch():
     assert B.rmsnorm_describe_plan(0, 65536, 4096, "bfloat16").startswith("tma cluster=1")
     assert B.rmsnorm_describe_plan(1, 65536, 4096, "bfloat16").startswith("tma cluster=1")
     assert B.rmsnorm_describe_plan(0, 16384, 16384, "float32").startswith("tma cluster=4")
-    # 32 KB rows: the forward splits them over a cluster, the backward keeps them
-    # in one 512-thread block
-    assert B.rmsnorm_describe_plan(0, 16384, 16384, "float16").startswith("tma cluster=2")
+    # 32 KB rows stay in one block: 256 threads x 8 vectors forward, 512 x 4 backward
+    assert B.rmsnorm_describe_plan(0, 16384, 16384, "float16").startswith("tma cluster=1 threads=256 vpt=8")
     assert B.rmsnorm_describe_plan(1, 16384, 16384, "float16").startswith("tma cluster=1 threads=512 vpt=4")
     assert B.rmsnorm_describe_plan(1, 16384, 8192, "float32").startswith("tma cluster=1 threads=512 vpt=4")
     assert B.rmsnorm_describe_plan(1, 16384, 16384, "float32").startswith("tma cluster=4")
