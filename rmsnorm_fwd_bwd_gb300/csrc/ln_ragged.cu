@@ -290,7 +290,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
         const float r = __shfl_sync(0xffffffffu, r_cur, static_cast<int>(j & 31));
         if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        // x_hat (zero outside the row) and u = dy * gamma (dy and gamma are zero there)
+        // x_hat and u = dy * gamma; outside the row x, dy and gamma are zero, so u and
+        // every product with dy vanish there whatever x_hat is (-mean * r), and
+        // those columns are never written: x_hat needs no mask
         float hf[VPT][VEC], uf[VPT][VEC];
         float p0 = 0.f, p1 = 0.f;
 #pragma unroll
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
             }
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                hf[v][e] = ((bits[v] >> e) & 1u) ? __fmul_rn(xf[e] - mu, r) : 0.f;
+                hf[v][e] = __fmul_rn(xf[e] - mu, r);
                 uf[v][e] = __fmul_rn(df[e], g[e]);
                 p0 += uf[v][e];
                 p1 = fmaf(uf[v][e], hf[v][e], p1);
