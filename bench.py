@@ -250,24 +250,37 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(sources=None) -> str:
+    """Digest of the kernel sources: the named files of csrc/ (their names and
+    contents), or every file there when sources is None."""
+    csrc = os.path.join(ROOT, "rmsnorm_fwd_bwd_gb300", "csrc")
+    paths = (sorted(glob.glob(os.path.join(csrc, "*"))) if sources is None
+             else [os.path.join(csrc, n) for n in sorted(sources)])
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "rmsnorm_fwd_bwd_gb300", "csrc", "*"))):
+    for p in paths:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+def recorded_traffic(kernel_key: str, path=None):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current
+    sources of the kernels it covers (the entry's "sources": the kernels' files, the
+    planner and the shared headers; every kernel file when absent)."""
+    path = path or os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel_key)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_digest") != kernel_source_digest():
+    if not rec:
+        return None
+    try:
+        digest = kernel_source_digest(rec.get("sources"))
+    except OSError:
+        return None
+    if rec.get("source_digest") != digest:
         return None
     return rec.get("dram_bytes_per_launch")
 

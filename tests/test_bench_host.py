@@ -80,3 +80,27 @@ def test_workload_table_and_bytes():
     assert (w.M, w.N, w.dtype) == (65536, 4096, "bfloat16")
     assert w.fwd_bytes() == 1_074_012_160
     assert w.bwd_bytes() == 1_610_891_264
+
+
+def test_recorded_traffic_follows_its_sources(tmp_path):
+    """A traffic record counts only while the files it names hash to its digest;
+    an unknown file or a stale digest gives null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    srcs = ["bwd.cu", "launch.h"]
+    rec = {"k": {"dram_bytes_per_launch": 123.0, "sources": srcs,
+                 "source_digest": bench.kernel_source_digest(srcs)}}
+    path = tmp_path / "t.json"
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k", path=str(path)) == 123.0
+    assert bench.recorded_traffic("missing", path=str(path)) is None
+    rec["k"]["source_digest"] = "0" * 16
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k", path=str(path)) is None
+    rec["k"]["sources"] = ["no_such_file.cu"]
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k", path=str(path)) is None
+    # without "sources" the digest covers every kernel file
+    rec = {"k": {"dram_bytes_per_launch": 7.0, "source_digest": bench.kernel_source_digest()}}
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k", path=str(path)) == 7.0
