@@ -188,14 +188,20 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
            !((static_cast<int64_t>(N) * s) / cl <= (cl == 1 ? max_slice_unsplit : kSliceMaxBytes) &&
              N % (cl * vec) == 0 && N / cl <= (cl == 1 ? max_cta_elems_unsplit : max_cta_elems)))
         cl *= 2;
-    const int tmax = cl == 1 ? (pass == 4 ? kDbwdMaxThreads : (pass == 1 ? kWideRowThreads : kTmaMaxThreads))
-                             : kTmaMaxThreads;
     if (cl > 4) return false;
+    // the double backward splits rows that need four CTAs over eight: 2048-element
+    // slices on 128 threads leave room for three blocks per SM, where four 256-thread
+    // slices held one (fp32 16384: 5057 -> 5456 GB/s)
+    if (pass == 4 && cl == 4 && N % (8 * vec) == 0) cl = 8;
+    // a cluster's warps all hand one partial per row to a 32-lane read, so a
+    // cluster holds at most 32 warps
+    const int tmax = cl == 1 ? (pass == 4 ? kDbwdMaxThreads : (pass == 1 ? kWideRowThreads : kTmaMaxThreads))
+                             : std::min(kTmaMaxThreads, 32 * 32 / cl);
     const int nvec = N / (cl * vec);
     const Override& ov = g_override[pass];
     int vpt = ov.vpt;
     if (vpt == 0) {
-        const int cap = ov.threads ? ov.threads : (cl > 1 ? kClusterThreadCap[pass] : kThreadCap[pass]);
+        const int cap = ov.threads ? ov.threads : (cl > 1 ? std::min(kClusterThreadCap[pass], tmax) : kThreadCap[pass]);
         for (vpt = kMinVpt; vpt <= 8; vpt *= 2)
             if (round_up(ceil_div(nvec, vpt), 32) <= cap) break;
         // rows wider than the thread cap holds at 8 vectors (the RMSNorm
@@ -218,7 +224,7 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
                                                             : kTmaMaxThreads;
     if (threads % 32 != 0 || threads > tbound) return false;
     if (static_cast<int64_t>(threads) * vpt < nvec) return false;
-    if (cl > 8) return false;
+    if (cl > 8 || (cl > 1 && (threads / 32) * cl > 32)) return false;
     const int slice = (N / cl) * s;
     const int stage = kInputs[pass] * slice;
     // warp partials [2][kPartials][32] floats, abort flag, fp32 per-column planes

@@ -65,8 +65,8 @@ SHAPES = [
     ("bfloat16", 300, 2048, "tma cluster=1"),
     ("bfloat16", 300, 4096, "tma cluster=1"),
     ("float32", 41, 8192, "tma cluster=2"),
-    ("bfloat16", 40, 16384, "tma cluster=4"),
-    ("float32", 24, 16384, "tma cluster=4"),
+    ("bfloat16", 40, 16384, "tma cluster=8"),
+    ("float32", 24, 16384, "tma cluster=8"),
     ("bfloat16", 67, 4099, "ragged"),
     ("float32", 50, 333, "ragged"),
     ("float16", 33, 1001, "ragged"),
