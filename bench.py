@@ -264,10 +264,11 @@ def kernel_source_digest(sources=None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key: str, path=None):
+def recorded_traffic(kernel_key: str, plan=None, path=None):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current
-    sources of the kernels it covers (the entry's "sources": the kernels' files, the
-    planner and the shared headers; every kernel file when absent)."""
+    sources of the kernels it covers (the entry's "sources": the kernels' files and
+    the shared headers; every kernel file when absent) and, when the entry records
+    one, with the launch plan `plan` (rmsnorm_describe_plan's text)."""
     path = path or os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -281,6 +282,8 @@ def recorded_traffic(kernel_key: str, path=None):
     except OSError:
         return None
     if rec.get("source_digest") != digest:
+        return None
+    if "plan" in rec and rec["plan"] != plan:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -497,8 +500,8 @@ def run_ours(args, w):
     fwd_avg_ms = statistics.mean(fwd_ms)
     bwd_gbs = w.bwd_bytes() / (bwd_avg_ms / 1e3) / 1e9
     fwd_gbs = w.fwd_bytes() / (fwd_avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic(f"{op.name}_bwd {w.name}")
     p_fwd, p_bwd = op.passes
+    traffic = recorded_traffic(f"{op.name}_bwd {w.name}", plan=B.rmsnorm_describe_plan(p_bwd, M, N, dt))
     line = {
         "metric": metric_for(w), "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / K, "higher_is_better": True,
@@ -656,7 +659,8 @@ def run_double_backward(args, w):
                  "plan": B.rmsnorm_describe_plan(4, M, N, dt)},
         "roofline": {"bound": "hbm", "kernel": "rmsnorm_bwd_bwd (fused row kernel + d_gamma reduce)",
                      "achieved": gbs, "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": recorded_traffic(f"rmsnorm_bwd_bwd {w.name}"),
+                     "frac": gbs / peak, "traffic": recorded_traffic(f"rmsnorm_bwd_bwd {w.name}",
+                                                                plan=B.rmsnorm_describe_plan(4, M, N, dt)),
                      "algorithmic_bytes": nbytes},
         "e2e": {"value": nbytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},

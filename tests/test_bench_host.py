@@ -104,3 +104,8 @@ def test_recorded_traffic_follows_its_sources(tmp_path):
     rec = {"k": {"dram_bytes_per_launch": 7.0, "source_digest": bench.kernel_source_digest()}}
     path.write_text(json.dumps(rec))
     assert bench.recorded_traffic("k", path=str(path)) == 7.0
+    # a recorded plan must match the current one
+    rec["k"]["plan"] = "tma cluster=1 threads=128"
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k", plan="tma cluster=1 threads=128", path=str(path)) == 7.0
+    assert bench.recorded_traffic("k", plan="tma cluster=2 threads=128", path=str(path)) is None
