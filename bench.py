@@ -184,6 +184,15 @@ def aggregate(bytes_per_step_per_rank: int, steps: int, world: int, max_seconds:
 # --------------------------------------------------------------------------- #
 # clocks
 # --------------------------------------------------------------------------- #
+def clock_log_path(args, rank: int) -> str:
+    """Where the raw clock samples of this rank go: --clock-log DIR, else the
+    system's temporary directory (the JSON line carries their summary)."""
+    import tempfile
+    d = args.clock_log or tempfile.gettempdir()
+    os.makedirs(d, exist_ok=True)
+    return os.path.join(d, f"clocks_rank{rank}.csv")
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -425,8 +434,7 @@ def run_ours(args, w):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    clocks = ClockSampler(local, clock_log_path(args, rank))
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
@@ -581,8 +589,7 @@ def run_double_backward(args, w):
     torch.cuda.synchronize()
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    clocks = ClockSampler(local, clock_log_path(args, rank))
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
@@ -682,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="directory for the raw nvidia-smi clock samples (default: the temporary directory)")
     ap.add_argument("--double-backward", action="store_true",
                     help="time the RMSNorm double backward on the workload instead of fwd+bwd")
     ap.add_argument("--rows", type=int, default=None,
