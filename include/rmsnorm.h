@@ -132,9 +132,10 @@ rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
  * anything is launched; on a 152-SM GB300 the measured workloads need at most
  * about 10 MiB.
  *
- * The first call on a device looks up the array's device address (a host-side
- * runtime query, no allocation); make that first call before any stream
- * capture. No call allocates. All calls on a device share the one array: two
+ * Every call looks up the array's device address in the current context (a
+ * host-side runtime query, no allocation), so a device reset between calls is
+ * harmless; the first call on a device also loads the library's code there,
+ * so make that first call before any stream capture. No call allocates. All calls on a device share the one array: two
  * calls whose kernels overlap on the GPU (for example on different streams
  * without ordering between them) race on it and give wrong dgamma. The array
  * keeps the last call's partial sums; nothing in it has to start at zero.
@@ -201,20 +202,6 @@ rmsnorm_status rmsnorm_selftest_wait_timeout(uint32_t polls, rmsnorm_stream_t st
  */
 rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, rmsnorm_dtype dtype,
                                      int aligned16, char* buf, size_t buf_len);
-
-/*
- * Tuning hook: override the TMA-path launch shape for one pass (0 = forward,
- * 1 = backward, 2 / 3 = LayerNorm forward / backward, 4 = double backward).
- * threads: threads per block (multiple of 32); vpt: 16-byte vectors per thread
- * (1 to 8; the aligned TMA path takes 1, 2, 4 or 8, the ragged one 1 to 6);
- * stages: pipeline depth; blocks_per_sm:
- * cap on resident blocks per SM. Any value 0 keeps the built-in choice;
- * all zeros restores the defaults. A shape that cannot hold the row makes the
- * following calls fail with RMSNORM_ERR_UNSUPPORTED. Process-wide, not
- * thread-safe against concurrent calls.
- */
-rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int stages,
-                                           int blocks_per_sm);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,9 @@ import re
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "librmsnorm.so")
+# RMSNORM_LIBRARY may name another build of this library (the debug build,
+# librmsnorm_debug.so, whose kernels check their reads); default: the release build.
+LIB_PATH = os.environ.get("RMSNORM_LIBRARY") or os.path.join(HERE, "librmsnorm.so")
 INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
 HEADER_PATH = os.path.join(INCLUDE_DIR, "rmsnorm.h")
 

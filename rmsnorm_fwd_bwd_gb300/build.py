@@ -17,6 +17,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm.so")
+# debug build: the same sources with -DRMSNORM_DEBUG (every TMA read of a row
+# kernel is checked against its tensor's extent; see csrc/device.cuh)
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "librmsnorm_debug.so")
 HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,21 +42,25 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link the release library, or with debug=True the debug
+    build (librmsnorm_debug.so); returns the library's path."""
+    build_dir, lib_path = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DRMSNORM_DEBUG"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + HEADERS
     nvcc = _nvcc()
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + headers):
             jobs.append((src, obj))
 
     def compile_one(job):
         src, obj = job
         log = obj[:-2] + ".ptxas.txt"
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj + ".tmp"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         with open(log, "w") as f:
             f.write(res.stdout + res.stderr)
@@ -64,18 +72,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(compile_one, jobs))
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources]
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in sources]
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".{os.getpid()}.tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr[-4000:]}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib_path)
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
+    build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv)

@@ -24,6 +24,7 @@
 #include "../../include/rmsnorm.h"
 #include "../../include/rmsnorm_double_backward.h"
 #include "launch.h"
+#include "tuning.h"
 
 namespace rmsnorm {
 
@@ -72,7 +73,6 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int smem_optin = 0;
-    uint32_t* err = nullptr;
 };
 
 struct Override {
@@ -101,7 +101,8 @@ const void* kernel_for(int pass, const Plan& p) {
     }
 }
 
-// Caller holds g_mu.
+// Caller holds g_mu. The device's SM count and shared-memory limit, read once
+// per device (properties of the hardware, unchanged by a device reset).
 bool device_info(int dev, DeviceInfo*& out) {
     if (dev < 0 || dev >= kMaxDevices) return false;
     DeviceInfo& d = g_dev[dev];
@@ -109,13 +110,22 @@ bool device_info(int dev, DeviceInfo*& out) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return false;
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return false;
-        d.err = static_cast<uint32_t*>(p);
         d.ready = true;
     }
     out = &d;
     return true;
+}
+
+// Device address of the error word in the current context, looked up on every
+// call (a host-side query): an address kept from before a device reset would
+// point into the destroyed context.
+uint32_t* error_word_address() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return static_cast<uint32_t*>(p);
 }
 
 // Caller holds g_mu. Allows the largest dynamic shared memory once per kernel and device.
@@ -132,6 +142,13 @@ bool prepare_kernel(const void* k, int dev, const DeviceInfo& di) {
         return false;
     g_attr_done[key] = true;
     return true;
+}
+
+// Caller holds g_mu. Forget the attributes set on `dev`'s kernels: after a
+// device reset they belong to the destroyed context and must be set again.
+void forget_kernel_attributes(int dev) {
+    for (auto it = g_attr_done.begin(); it != g_attr_done.end();)
+        it = it->first.second == dev ? g_attr_done.erase(it) : std::next(it);
 }
 
 // Resident blocks per SM (cluster == 1) or resident clusters on the device.
@@ -572,18 +589,49 @@ rmsnorm_status current_device(int& dev, DeviceInfo*& di) {
     return RMSNORM_OK;
 }
 
+// The launch plan of one call, chosen under g_mu; the launches that follow run
+// without the lock, so callers on different streams do not wait for each
+// other's launches.
+struct CallPlan {
+    int dev = 0;
+    Plan plan;
+    uint32_t* err = nullptr;  // device error word of the current context
+};
+
+rmsnorm_status plan_call(int pass, int64_t M, int N, int dt, int offset, int layout, CallPlan& c) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo* di = nullptr;
+    rmsnorm_status st = current_device(c.dev, di);
+    if (st != RMSNORM_OK) return st;
+    if (!get_plan(pass, M, N, dt, offset, layout, c.dev, *di, c.plan)) return RMSNORM_ERR_UNSUPPORTED;
+    c.err = error_word_address();
+    return c.err ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+// Launch the row kernel of `pass`. A failed launch is retried once after the
+// kernel's attributes are set again: launch attributes (the opt-in shared-memory
+// size) belong to a CUDA context, and a device reset since the first call on
+// this device discards them while the library's record of them survives.
+cudaError_t launch_pass(int pass, const CallPlan& c, const RowArgs& a, cudaStream_t s) {
+    const void* k = kernel_for(pass, c.plan);
+    if (!k) return cudaErrorInvalidDeviceFunction;
+    cudaError_t e = launch_rows(k, c.plan, a, s);
+    if (e == cudaSuccess) return e;
+    (void)cudaGetLastError();
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceInfo* di = nullptr;
+        int dev = 0;
+        if (current_device(dev, di) != RMSNORM_OK) return cudaErrorInvalidDevice;
+        forget_kernel_attributes(dev);
+        if (!prepare_kernel(k, dev, *di)) return cudaErrorInvalidValue;
+    }
+    return launch_rows(k, c.plan, a, s);
+}
+
 }  // namespace
 
-uint32_t* device_error_word() {
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
-    if (current_device(dev, di) != RMSNORM_OK) {
-        (void)cudaGetLastError();
-        return nullptr;
-    }
-    return di->err;
-}
+uint32_t* device_error_word() { return error_word_address(); }
 
 }  // namespace rmsnorm
 
@@ -613,12 +661,8 @@ rmsnorm_status fwd_impl(const void* x, int64_t ldx, const void* gamma, void* y, 
     const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16) && (ldx * s) % 16 == 0 &&
                      (ldy * s) % 16 == 0;
     const int layout = a16 ? kLayoutAligned : kLayoutPhase;
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(0, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    CallPlan c;
+    if ((st = plan_call(0, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
     RowArgs a = {};
     a.x = x;
     a.gamma = gamma;
@@ -629,9 +673,9 @@ rmsnorm_status fwd_impl(const void* x, int64_t ldx, const void* gamma, void* y, 
     a.ldx = ldx;
     a.ldy = ldy;
     a.eps = eps;
-    a.stages = p.stages;
-    a.err = di->err;
-    if (launch_fwd(p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    a.stages = c.plan.stages;
+    a.err = c.err;
+    if (launch_pass(0, c, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -646,11 +690,7 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     if (!dgamma) return RMSNORM_ERR_NULL;
     if (!aligned(dgamma, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
     if (M == 0) {
-        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
         if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
@@ -667,9 +707,9 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15) &&
                             (ldx * s) % 16 == (lddy * s) % 16;
     const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(1, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    CallPlan c;
+    if ((st = plan_call(1, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
+    const Plan& p = c.plan;
     const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -685,8 +725,8 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     a.lddy = lddy;
     a.lddx = lddx;
     a.stages = p.stages;
-    a.err = di->err;
-    if (launch_bwd(p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    a.err = c.err;
+    if (launch_pass(1, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
@@ -708,13 +748,10 @@ rmsnorm_status ln_fwd_impl(const void* x, int64_t ldx, const void* gamma, const 
     // each row's own phase, y written at any phase)
     const bool a16 = aligned(x, 16) && aligned(gamma, 16) && aligned(beta, 16) && aligned(y, 16) &&
                      (ldx * s) % 16 == 0 && (ldy * s) % 16 == 0;
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(2, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutPhase, dev, *di, p))
-        return RMSNORM_ERR_UNSUPPORTED;
+    CallPlan c;
+    if ((st = plan_call(2, M, static_cast<int>(N), dtype, 0, a16 ? kLayoutAligned : kLayoutPhase, c)) !=
+        RMSNORM_OK)
+        return st;
     RowArgs a = {};
     a.x = x;
     a.gamma = gamma;
@@ -727,10 +764,9 @@ rmsnorm_status ln_fwd_impl(const void* x, int64_t ldx, const void* gamma, const 
     a.ldx = ldx;
     a.ldy = ldy;
     a.eps = eps;
-    a.stages = p.stages;
-    a.err = di->err;
-    if (launch_rows(kernel_for(2, p), p, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return RMSNORM_ERR_CUDA;
+    a.stages = c.plan.stages;
+    a.err = c.err;
+    if (launch_pass(2, c, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -745,11 +781,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     if (!dgamma || !dbeta) return RMSNORM_ERR_NULL;
     if (!aligned(dgamma, s) || !aligned(dbeta, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
     if (M == 0) {
-        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
         if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs, dbeta) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
@@ -765,9 +797,9 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     const bool same_phase = (reinterpret_cast<uintptr_t>(x) & 15) == (reinterpret_cast<uintptr_t>(dy) & 15) &&
                             (ldx * s) % 16 == (lddy * s) % 16;
     const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    CallPlan c;
+    if ((st = plan_call(3, M, static_cast<int>(N), dtype, 0, layout, c)) != RMSNORM_OK) return st;
+    const Plan& p = c.plan;
     const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -784,8 +816,8 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     a.lddy = lddy;
     a.lddx = lddx;
     a.stages = p.stages;
-    a.err = di->err;
-    if (launch_rows(kernel_for(3, p), p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    a.err = c.err;
+    if (launch_pass(3, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs, dbeta) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
@@ -804,11 +836,7 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     if (!d_gamma) return RMSNORM_ERR_NULL;
     if (!aligned(d_gamma, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    DeviceInfo* di = nullptr;
     if (M == 0) {
-        if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
         if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), d_gamma, cs) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
@@ -829,9 +857,9 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
                             (reinterpret_cast<uintptr_t>(ddx) & 15) == ph && (ldx * s) % 16 == (lddy * s) % 16 &&
                             (ldx * s) % 16 == (ldddx * s) % 16;
     const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
-    if ((st = current_device(dev, di)) != RMSNORM_OK) return st;
-    Plan p;
-    if (!get_plan(4, M, static_cast<int>(N), dtype, offset, layout, dev, *di, p)) return RMSNORM_ERR_UNSUPPORTED;
+    CallPlan c;
+    if ((st = plan_call(4, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
+    const Plan& p = c.plan;
     const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
@@ -852,8 +880,8 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     a.ldd_dy = ldd_dy;
     a.lddx = ldd_x;
     a.stages = p.stages;
-    a.err = di->err;
-    if (launch_rows(kernel_for(4, p), p, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    a.err = c.err;
+    if (launch_pass(4, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, d_gamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }

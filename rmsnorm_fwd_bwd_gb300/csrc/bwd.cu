@@ -87,8 +87,9 @@ __global__ void __launch_bounds__(BwdTmaBounds<DT, VPT, CLUSTER>::threads, (BwdT
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
         const size_t r = static_cast<size_t>(cid + j * ncl);
         mbar_arrive_expect_tx(bar, stage_bytes);
-        bulk_g2s(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol);
+        bulk_g2s_in(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol,
+                    a.dy, a.M, a.lddy, a.N, E::kBytes, a.err);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;
@@ -302,55 +303,101 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
     }
 }
 
-// dgamma[j] = sum_{p < units} ws[p][j] in a fixed order. A block owns 32
-// columns; thread (cq, ry) owns columns 4cq..4cq+3 of them and sums rows
-// ry, ry + 32, ... in sequence (8 threads read 128 contiguous bytes of a row);
-// then thread cq adds the 32 row-lane sums in ry order. units == 0 (no rows)
-// writes zeros. Rows of N % 4 != 0 floats are read one column at a time.
-// blockIdx.y = 1 sums the second plane (LayerNorm's dbeta partials) into out1.
+// dgamma[j] = sum_{p < units} ws[p][j] in a fixed order, without atomics.
+// A 32-column tile of the partial rows is summed by a cluster of R CTAs
+// (blockIdx.y = rank, R = gridDim.y); CTA k takes the contiguous chunk
+// [k*chunk, (k+1)*chunk) of the rows. In a CTA, lane (cq, rq) of warp w owns
+// columns 4cq..4cq+3 and rows ry = 4w + rq, ry + 32, ... of the chunk; a warp
+// reads 4 rows x 128 contiguous bytes per step, and each thread issues up to
+// kReduceBatch loads before adding any of them, so a launch keeps every row of
+// the workspace in flight at once (the partial rows were just written and sit
+// in L2: the kernel is latency-bound, not bandwidth-bound). The row sums are
+// then combined in a fixed tree: in row order within a thread, a butterfly over
+// the 4 row lanes of a warp, the 8 warps in order through shared memory, and
+// the R CTAs in rank order through distributed shared memory; the result is
+// rounded once into the I/O dtype. The order depends only on (units, N), so
+// dgamma is bitwise reproducible. units == 0 (no rows) writes zeros. Rows of
+// N % 4 != 0 floats are read one column at a time. blockIdx.z = 1 sums the
+// second plane (LayerNorm's dbeta partials) into out1.
+constexpr int kReduceBatch = 4;
 template <int DT>
 __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
                                                            void* out0, void* out1) {
     using E = Elem<DT>;
-    __shared__ float4 part[32][8];
-    const int cq = threadIdx.x & 7;
-    const int ry = threadIdx.x >> 3;
+    __shared__ float4 part[8][8];
+    __shared__ float cpart[32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int cq = lane & 7;
+    const int ry = warp * 4 + (lane >> 3);
     const int col = blockIdx.x * 32 + cq * 4;
-    void* dgamma = blockIdx.y == 0 ? out0 : out1;
-    if (blockIdx.y != 0) ws += units * static_cast<int64_t>(N);
+    const int R = static_cast<int>(gridDim.y);
+    const int rank = static_cast<int>(blockIdx.y);
+    void* dgamma = blockIdx.z == 0 ? out0 : out1;
+    if (blockIdx.z != 0) ws += units * static_cast<int64_t>(N);
+    const int64_t chunk = (units + R - 1) / R;
+    const int64_t p0 = rank * chunk;
+    const int64_t p1 = p0 + chunk < units ? p0 + chunk : units;
     griddep_wait();  // the partial sums come from the row kernel just before
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if ((N & 3) == 0) {
-        if (col < N) {
-#pragma unroll 4
-            for (int64_t p = ry; p < units; p += 32) {
-                const float4 v = *reinterpret_cast<const float4*>(ws + p * N + col);
-                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    const bool vec = (N & 3) == 0;
+    for (int64_t base = p0 + ry; base < p1; base += 32 * kReduceBatch) {
+        float4 v[kReduceBatch];
+#pragma unroll
+        for (int i = 0; i < kReduceBatch; ++i) {
+            const int64_t p = base + 32 * i;
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p < p1) {
+                const float* rowp = ws + p * N;
+                if (vec) {
+                    if (col < N) v[i] = __ldcg(reinterpret_cast<const float4*>(rowp + col));
+                } else {
+                    if (col < N) v[i].x = __ldcg(rowp + col);
+                    if (col + 1 < N) v[i].y = __ldcg(rowp + col + 1);
+                    if (col + 2 < N) v[i].z = __ldcg(rowp + col + 2);
+                    if (col + 3 < N) v[i].w = __ldcg(rowp + col + 3);
+                }
             }
         }
-    } else {
-#pragma unroll 2
-        for (int64_t p = ry; p < units; p += 32) {
-            const float* rowp = ws + p * N;
-            if (col < N) s.x += rowp[col];
-            if (col + 1 < N) s.y += rowp[col + 1];
-            if (col + 2 < N) s.z += rowp[col + 2];
-            if (col + 3 < N) s.w += rowp[col + 3];
+#pragma unroll
+        for (int i = 0; i < kReduceBatch; ++i) {
+            if (base + 32 * i < p1) {
+                s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w;
+            }
         }
     }
-    part[ry][cq] = s;
+    // the 4 row lanes of this warp (lanes cq, cq + 8, cq + 16, cq + 24)
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) {
+        s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+        s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+        s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+        s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+    }
+    if (lane < 8) part[warp][lane] = s;
     __syncthreads();
-    if (ry == 0) {
-        float4 t = part[0][cq];
-        for (int k = 1; k < 32; ++k) {
-            const float4 v = part[k][cq];
-            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+    if (threadIdx.x < 8) {
+        float4 t = part[0][threadIdx.x];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            const float4 u = part[w][threadIdx.x];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
-        if (col < N) E::st(dgamma, col, t.x);
-        if (col + 1 < N) E::st(dgamma, col + 1, t.y);
-        if (col + 2 < N) E::st(dgamma, col + 2, t.z);
-        if (col + 3 < N) E::st(dgamma, col + 3, t.w);
+        cpart[4 * threadIdx.x] = t.x;
+        cpart[4 * threadIdx.x + 1] = t.y;
+        cpart[4 * threadIdx.x + 2] = t.z;
+        cpart[4 * threadIdx.x + 3] = t.w;
     }
+    if (R > 1) cluster_sync(); else __syncthreads();
+    if (rank == 0 && threadIdx.x < 32) {
+        float t = cpart[threadIdx.x];
+        for (int k = 1; k < R; ++k)
+            t += dsmem_ld_f32(dsmem_map(smem_u32(&cpart[threadIdx.x]), static_cast<uint32_t>(k)));
+        const int c = blockIdx.x * 32 + threadIdx.x;
+        if (c < N) E::st(dgamma, c, t);
+    }
+    // no CTA leaves while rank 0 may still read its shared memory
+    if (R > 1) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -401,12 +448,6 @@ const void* dgamma_reduce_kernel_ptr(int dtype) {
     }
 }
 
-cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
-    const void* k = bwd_kernel(p);
-    if (!k) return cudaErrorInvalidDeviceFunction;
-    return launch_rows(k, p, a, s);
-}
-
 cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
@@ -435,16 +476,25 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
                                  cudaStream_t s, void* dbeta) {
     const void* k = dgamma_reduce_kernel_ptr(dtype);
     if (!k) return cudaErrorInvalidDeviceFunction;
+    // CTAs per column tile: enough that a thread issues at most 4 loads
+    // (rows / (32 x 4)), at most 8 (a portable cluster)
+    int64_t r = (units + 127) / 128;
+    if (r < 1) r = 1;
+    if (r > 8) r = 8;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), dbeta ? 2u : 1u, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>((N + 31) / 32), static_cast<unsigned>(r), dbeta ? 2u : 1u);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = static_cast<unsigned>(r);
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma, &dbeta};
     return cudaLaunchKernelExC(&cfg, k, params);
 }

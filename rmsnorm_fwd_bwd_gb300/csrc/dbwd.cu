@@ -91,9 +91,11 @@ __global__ void __launch_bounds__(DbwdTmaThreads<VPT, CLUSTER>::value) dbwd_tma_
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
         const size_t r = static_cast<size_t>(cid + j * ncl);
         mbar_arrive_expect_tx(bar, stage_bytes);
-        bulk_g2s(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol);
-        bulk_g2s(smem_u32(st + 2 * slice_bytes), tsl + r * t_pitch, slice_bytes, bar, pol);
+        bulk_g2s_in(smem_u32(st), xsl + r * x_pitch, slice_bytes, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + slice_bytes), dysl + r * dy_pitch, slice_bytes, bar, pol,
+                    a.dy, a.M, a.lddy, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + 2 * slice_bytes), tsl + r * t_pitch, slice_bytes, bar, pol,
+                    a.ddx, a.M, a.ldddx, a.N, E::kBytes, a.err);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;

@@ -70,9 +70,11 @@ __global__ void __launch_bounds__(kRaggedDbwdMaxThreads) dbwd_ragged_kernel(cons
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
         const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
         mbar_arrive_expect_tx(bar, 3 * span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + 2 * stride), tb + row * t_pitch - o, span, bar, pol);
+        bulk_g2s_in(smem_u32(st), xb + row * x_pitch - o, span, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol,
+                    a.dy, a.M, a.lddy, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + 2 * stride), tb + row * t_pitch - o, span, bar, pol,
+                    a.ddx, a.M, a.ldddx, a.N, E::kBytes, a.err);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;

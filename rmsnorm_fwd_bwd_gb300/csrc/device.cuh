@@ -13,6 +13,14 @@ namespace rmsnorm {
 
 // Bit 0 of the device error word: an mbarrier wait ran out of polls.
 constexpr uint32_t kDevErrWaitTimeout = 1u;
+// Bit 1 (debug builds, -DRMSNORM_DEBUG): a row kernel was about to read bytes
+// outside the tensor it reads; the read was skipped.
+constexpr uint32_t kDevErrOutOfBounds = 2u;
+#ifdef RMSNORM_DEBUG
+constexpr bool kDebugReads = true;
+#else
+constexpr bool kDebugReads = false;
+#endif
 // Polls of mbarrier.try_wait before a wait gives up. Each poll may suspend the
 // thread for a hardware-defined interval, so this bounds a wait to well under
 // a few seconds while never firing on a healthy pipeline.
@@ -175,6 +183,35 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// True when [p, p + bytes) lies in the 16-byte chunks that hold at least one
+// byte of the row-major tensor at `base` (M rows of N elements of `elem` bytes,
+// rows `ld` elements apart): [floor16(base), ceil16(end of the last row)). A
+// copy of a row's aligned span may take the neighbouring bytes of its first
+// and last chunk, never a chunk outside the tensor.
+__device__ __forceinline__ bool read_in_tensor(const void* p, uint32_t bytes, const void* base, int64_t M,
+                                               int64_t ld, int N, int elem) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t lo = b & ~uintptr_t(15);
+    const uintptr_t hi = (b + static_cast<uintptr_t>(((M - 1) * ld + N) * elem) + 15) & ~uintptr_t(15);
+    const uintptr_t q = reinterpret_cast<uintptr_t>(p);
+    return M > 0 && q >= lo && q + bytes <= hi;
+}
+
+// TMA bulk copy of bytes of the tensor described by (base, M, ld, N, elem). In
+// debug builds the source range is checked first: outside the tensor, the copy
+// is skipped and kDevErrOutOfBounds set (the stage's mbarrier then never
+// completes, its bounded wait gives up and the kernel takes its abort path). In
+// other builds the check compiles away.
+__device__ __forceinline__ void bulk_g2s_in(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                            uint64_t policy, const void* base, int64_t M, int64_t ld, int N,
+                                            int elem, uint32_t* err) {
+    if (kDebugReads && !read_in_tensor(src, bytes, base, M, ld, N, elem)) {
+        atomicOr(err, kDevErrOutOfBounds);
+        return;
+    }
+    bulk_g2s(dst, src, bytes, bar, policy);
 }
 
 // ---------------------------------------------------------------------------

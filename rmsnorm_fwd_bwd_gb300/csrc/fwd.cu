@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
         for (int64_t j = 0; j < pre; ++j) {
             const uint32_t bar = smem_u32(&full[j]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
-                     slice_bytes, bar, pol);
+            bulk_g2s_in(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
+                        slice_bytes, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
         }
     }
 
@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
             fence_proxy_async_smem();
             const uint32_t bar = smem_u32(&full[s]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * x_pitch, slice_bytes, bar, pol);
+            bulk_g2s_in(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * x_pitch, slice_bytes, bar, pol,
+                        a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
         }
         if (++s == S) {
             s = 0;
@@ -304,12 +305,6 @@ const void* fwd_kernel(const Plan& p) {
     if (p.path == kPathRowVec) return rowvec_kernel(0, p);
     if (p.path == kPathRagged) return ragged_kernel(0, p);
     return p.offset ? fwd_pick<true>(p) : fwd_pick<false>(p);
-}
-
-cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s) {
-    const void* k = fwd_kernel(p);
-    if (!k) return cudaErrorInvalidDeviceFunction;
-    return launch_rows(k, p, a, s);
 }
 
 }  // namespace rmsnorm

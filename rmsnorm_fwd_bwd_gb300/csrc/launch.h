@@ -91,8 +91,6 @@ const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward
 const void* dbwd_ragged_kernel_ptr(const Plan& p);    // its ragged TMA kernel
 const void* dgamma_reduce_kernel_ptr(int dtype);
 
-cudaError_t launch_fwd(const Plan& p, const RowArgs& a, cudaStream_t s);
-cudaError_t launch_bwd(const Plan& p, const RowArgs& a, cudaStream_t s);
 // Launch `k` with the plan's grid, block, shared memory and cluster shape, and
 // programmatic stream serialization.
 cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s);
@@ -101,7 +99,8 @@ cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStre
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
                                  cudaStream_t s, void* dbeta = nullptr);
 
-// Device address of the error word on the current device (nullptr on failure).
+// Device address of the error word in the current context (nullptr on failure),
+// looked up on every call.
 uint32_t* device_error_word();
 
 }  // namespace rmsnorm

@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
         for (int64_t j = 0; j < pre; ++j) {
             const uint32_t bar = smem_u32(&full[j]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
-                     slice_bytes, bar, pol);
+            bulk_g2s_in(smem_u32(ring + j * slice_bytes), xsl + static_cast<size_t>(cid + j * ncl) * x_pitch,
+                        slice_bytes, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
         }
     }
 
@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_fwd_tma_kernel(const RowArg
             fence_proxy_async_smem();
             const uint32_t bar = smem_u32(&full[s]);
             mbar_arrive_expect_tx(bar, slice_bytes);
-            bulk_g2s(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * x_pitch, slice_bytes, bar, pol);
+            bulk_g2s_in(smem_u32(st), xsl + static_cast<size_t>(row + S * ncl) * x_pitch, slice_bytes, bar, pol,
+                        a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
         }
         if (++s == S) {
             s = 0;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads, 3) ln_fwd_ragged_kernel(const 
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
         const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
         mbar_arrive_expect_tx(bar, span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
+        bulk_g2s_in(smem_u32(st), xb + row * x_pitch - o, span, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;
@@ -248,8 +248,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
     auto issue = [&](int64_t j, const unsigned char* st, uint32_t bar) {
         const size_t row = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(j) * gridDim.x;
         mbar_arrive_expect_tx(bar, 2 * span);
-        bulk_g2s(smem_u32(st), xb + row * x_pitch - o, span, bar, pol);
-        bulk_g2s(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol);
+        bulk_g2s_in(smem_u32(st), xb + row * x_pitch - o, span, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
+        bulk_g2s_in(smem_u32(st + stride), dyb + row * dy_pitch - o, span, bar, pol,
+                    a.dy, a.M, a.lddy, a.N, E::kBytes, a.err);
     };
     if (tid == 0) {
         const int64_t pre = nrows < S ? nrows : S;

@@ -5,14 +5,11 @@
 // scratch is a fixed-size array in the library's own device memory instead of
 // a caller buffer, and the call goes through the same validation, launch plan
 // and kernels as rmsnorm_bwd.
-#include <mutex>
-
 #include "../../include/rmsnorm.h"
 #include <cuda_runtime.h>
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr size_t kScratchFloats = RMSNORM_STATIC_SCRATCH_BYTES / sizeof(float);
 
 // One copy per device that loads the library, held until the process exits.
@@ -20,28 +17,19 @@ constexpr size_t kScratchFloats = RMSNORM_STATIC_SCRATCH_BYTES / sizeof(float);
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) float g_bwd_scratch[kScratchFloats];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_bwd_scratch on the current device, looked up once per
-// device (the first call on a device does the lookup).
+// Device address of g_bwd_scratch in the current context. Looked up on every
+// call: the lookup is a host-side runtime query that allocates nothing, and an
+// address kept from an earlier call would be stale after a device reset (the
+// array then lives in a new context, possibly at another address). The first
+// call on a device also loads the library's module there, which is why that
+// first call should come before any stream capture.
 rmsnorm_status scratch_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) {
         (void)cudaGetLastError();
         return RMSNORM_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return RMSNORM_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();
-            return RMSNORM_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return RMSNORM_OK;
 }
 
