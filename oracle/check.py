@@ -20,8 +20,12 @@ def _rel_bound(dtype: str):
     return gate.FP32_MAX_RELATIVE_ERROR if dtype == "float32" else None
 
 
+def _whole(fn, *row_arrays):
+    return fn(*row_arrays)
+
+
 def gate_outputs(x, g, dy, dtype, offset, eps, y=None, rstd=None, dx=None, dgamma=None,
-                 rows=None, row_groups=None):
+                 rows=None, row_groups=None, map_rows=None):
     """Gate whichever target outputs are given.
 
     x, g, dy: full inputs (storage form). y, rstd, dx: target outputs for all
@@ -29,16 +33,21 @@ def gate_outputs(x, g, dy, dtype, offset, eps, y=None, rstd=None, dx=None, dgamm
     dgamma: target dgamma over all rows. ``row_groups``: optional {name: row
     indices into the gated rows}; each group is gated on its own as well (a
     stricter check where row classes have very different scales).
+    ``map_rows(fn, *row_arrays)``: optional way to evaluate the per-row oracle
+    functions (y, rstd, dx), e.g. over row chunks in several threads; it must
+    return what ``fn(*row_arrays)`` returns. Every row of those functions is
+    computed on its own, so splitting rows does not change a single value.
     Returns a list of ``gate.GateResult``.
     """
     out = []
     xs = x if rows is None else np.ascontiguousarray(x[rows])
     dys = dy if rows is None else np.ascontiguousarray(dy[rows])
     rel = _rel_bound(dtype)
+    rowwise = map_rows or _whole
     need_rows = y is not None or rstd is not None or dx is not None
     if need_rows:
-        yg, rg = orc.fwd_golden(xs, g, dtype, eps=eps, offset=offset, want_y=y is not None)
-        yr, rr = orc.fwd_reference(xs, g, dtype, eps=eps, offset=offset)
+        yg, rg = rowwise(lambda xx: orc.fwd_golden(xx, g, dtype, eps=eps, offset=offset, want_y=y is not None), xs)
+        yr, rr = rowwise(lambda xx: orc.fwd_reference(xx, g, dtype, eps=eps, offset=offset), xs)
         tensors = []
         if y is not None:
             tensors.append(("y", yg, orc.decode(yr, dtype), orc.decode(y, dtype), dtype))
@@ -46,8 +55,8 @@ def gate_outputs(x, g, dy, dtype, offset, eps, y=None, rstd=None, dx=None, dgamm
             tensors.append(("rstd", rg, rr.astype(np.float64), np.asarray(rstd, np.float64),
                             "float32"))
         if dx is not None:
-            dxg, _ = orc.bwd_golden(dys, xs, g, dtype, eps=eps, offset=offset)
-            dxr, _ = orc.bwd_reference(dys, xs, g, dtype, eps=eps, offset=offset)
+            dxg = rowwise(lambda dd, xx: orc.bwd_golden(dd, xx, g, dtype, eps=eps, offset=offset)[0], dys, xs)
+            dxr = rowwise(lambda dd, xx: orc.bwd_reference(dd, xx, g, dtype, eps=eps, offset=offset)[0], dys, xs)
             tensors.append(("dx", dxg, orc.decode(dxr, dtype), orc.decode(dx, dtype), dtype))
         for name, gold, ref, tgt, odt in tensors:
             out.append(gate.check(name, gold, ref, tgt, odt, rel_bound=rel if name != "rstd" else

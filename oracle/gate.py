@@ -194,3 +194,54 @@ def worst_index(golden: np.ndarray, target: np.ndarray) -> int:
     d = np.abs(np.asarray(target, np.float64) - np.asarray(golden, np.float64))
     d[~np.isfinite(d)] = -1.0
     return int(np.argmax(d))
+
+
+# --------------------------------------------------------------------------- #
+# the secondary closeness check (reported beside the gate, not instead of it)
+# --------------------------------------------------------------------------- #
+# Page "Check an AI model calculation before accelerating it", section
+# "Measurements before results" ("Three distinct numerical comparisons"): each
+# output and gradient is compared with the same-dtype reference element by
+# element, |value - reference| <= atol + rtol * |reference|, with tolerances
+# declared before the comparison: atol = 1e-5, rtol = 1e-4 for FP32 and
+# atol = rtol = 3e-3 for FP16. The page declares none for bfloat16.
+ALLCLOSE_TOLERANCES = {"float32": (1e-5, 1e-4), "float16": (3e-3, 3e-3)}
+
+
+@dataclass
+class CloseResult:
+    tensor: str
+    dtype: str
+    atol: float
+    rtol: float
+    elements: int
+    failing: int
+    worst_excess: float  # max over elements of |t - r| - (atol + rtol*|r|); <= 0 when all pass
+
+    @property
+    def passed(self) -> bool:
+        return self.failing == 0
+
+
+def allowed_difference(reference, dtype: str):
+    """atol + rtol * |reference| for the dtype's declared tolerances."""
+    atol, rtol = ALLCLOSE_TOLERANCES[dtype]
+    return atol + rtol * np.abs(np.asarray(reference, np.float64))
+
+
+def allclose(tensor: str, target, reference, dtype: str) -> CloseResult:
+    """The page's closeness rule on two arrays of decoded values (fp64 holding
+    the low-precision results). NaN only matches NaN; an infinity only matches
+    the same infinity."""
+    atol, rtol = ALLCLOSE_TOLERANCES[dtype]
+    t = np.asarray(target, np.float64).ravel()
+    r = np.asarray(reference, np.float64).ravel()
+    same_special = (np.isnan(t) & np.isnan(r)) | (np.isinf(t) & (t == r))
+    with np.errstate(invalid="ignore"):
+        excess = np.abs(t - r) - allowed_difference(r, dtype)
+    excess = np.where(same_special, -np.inf, excess)
+    excess = np.where(np.isnan(excess), np.inf, excess)
+    failing = int(np.count_nonzero(excess > 0))
+    worst = float(np.max(excess)) if excess.size else float("-inf")
+    return CloseResult(tensor, dtype, atol, rtol, int(t.size), failing, worst)
+
