@@ -48,6 +48,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
+# Nominal HBM3e bandwidth of a GB300 (~8 TB/s); the >= 85 % target is stated
+# against this figure, while frac_of_peak uses the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
 METRIC = "RMSNorm fwd/bwd HBM GB/s & % of peak, bf16 M=65536 N=4096, 1 GB300"
 
 
@@ -97,6 +100,12 @@ class RmsOp:
         orc.fwd_reference(x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
         orc.bwd_reference(dy, x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
 
+    def golden_step(self, orc, h, a, rows):
+        w = self.w
+        x, dy = h["x"][a:a + rows], h["dy"][a:a + rows]
+        orc.fwd_golden(x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
+        orc.bwd_golden(dy, x, h["g"], w.dtype, eps=w.eps, offset=w.offset)
+
     def step_bytes(self, rows):
         s, N = self.w.elem_bytes, self.w.N
         return (2 * rows * N * s + N * s + 4 * rows) + (3 * rows * N * s + 2 * N * s + 4 * rows)
@@ -133,6 +142,12 @@ class LnOp(RmsOp):
         x, dy = h["x"][a:a + rows], h["dy"][a:a + rows]
         orc.ln_fwd_reference(x, h["g"], h["b"], w.dtype, eps=w.eps)
         orc.ln_bwd_reference(dy, x, h["g"], w.dtype, eps=w.eps)
+
+    def golden_step(self, orc, h, a, rows):
+        w = self.w
+        x, dy = h["x"][a:a + rows], h["dy"][a:a + rows]
+        orc.ln_fwd_golden(x, h["g"], h["b"], w.dtype, eps=w.eps)
+        orc.ln_bwd_golden(dy, x, h["g"], w.dtype, eps=w.eps)
 
     def step_bytes(self, rows):
         s, N = self.w.elem_bytes, self.w.N
@@ -297,23 +312,65 @@ def recorded_traffic(kernel_key: str, plan=None, path=None):
     return rec.get("dram_bytes_per_launch")
 
 
-def cpu_oracle_rate(w, h, budget_s: float):
-    """Time the oracle's fp32-intermediate reference (fwd + bwd) on a row sample sized
-    to about budget_s seconds. h: the workload's host inputs. Returns (GB/s of
-    algorithmic bytes, rows, seconds)."""
+def host_cores() -> int:
+    """Cores in this process's affinity mask."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def run_oracle_rows(step, orc, h, start: int, rows: int, threads: int) -> None:
+    """step(orc, h, a, r) over rows [start, start + rows), split into contiguous
+    chunks on `threads` threads. The oracle's C calls release the GIL (ctypes),
+    so the chunks run in parallel; each chunk's dgamma is its own partial sum
+    (combining a few N-vectors is negligible next to the rows)."""
+    threads = max(1, min(threads, rows))
+    if threads == 1:
+        step(orc, h, start, rows)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    bounds = [(start + rows * i // threads, start + rows * (i + 1) // threads) for i in range(threads)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda ab: step(orc, h, ab[0], ab[1] - ab[0]), bounds))
+
+
+def oracle_rate(w, h, step, threads: int, budget_s: float):
+    """Time `step` (the fp32 reference or the fp64 golden, fwd + bwd) on a row
+    sample sized to about budget_s seconds on `threads` threads. Returns (GB/s
+    of algorithmic bytes, rows, seconds)."""
     from oracle import oracle as orc
     op = op_for(w)
+    orc.build()
 
     def run(rows):
         t = time.perf_counter()
-        op.oracle_step(orc, h, 0, rows)
+        run_oracle_rows(step, orc, h, 0, rows, threads)
         return time.perf_counter() - t
 
-    probe = min(64, w.M)
+    probe = min(64 * threads, w.M)
     t = run(probe)
     rows = int(min(w.M, max(probe, probe * budget_s / max(t, 1e-6))))
     t = run(rows)
     return op.step_bytes(rows) / t / 1e9, rows, t
+
+
+def cpu_baseline(w, h, budget_s: float):
+    """The CPU oracle on this host: the fp32-intermediate reference on every core
+    of the affinity mask (the headline figure) and on one thread, and the fp64
+    golden on every core, each on a bounded row sample of the workload."""
+    op = op_for(w)
+    cores = host_cores()
+    rate, rows, t = oracle_rate(w, h, op.oracle_step, cores, budget_s / 3)
+    rate1, rows1, t1 = oracle_rate(w, h, op.oracle_step, 1, budget_s / 3)
+    rateg, rowsg, tg = oracle_rate(w, h, op.golden_step, cores, budget_s / 3)
+    return {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} rows of the workload, fwd+bwd fp32-intermediate reference, "
+                      f"rows split over {cores} threads, {t:.1f} s",
+            "single_thread": {"value": rate1, "unit": "GB/s", "cores": 1,
+                              "sample": f"first {rows1} rows, {t1:.1f} s"},
+            "golden_fp64": {"value": rateg, "unit": "GB/s", "cores": cores,
+                            "sample": f"first {rowsg} rows, fwd+bwd fp64 golden, {tg:.1f} s"}}
 
 
 # --------------------------------------------------------------------------- #
@@ -327,27 +384,29 @@ def run_reference(args, w):
     op = op_for(w)
     h = op.host_inputs()
     orc.build()
+    cores = host_cores()
     total_budget = 60.0
-    probe = 64
+    probe = min(w.M, 64 * cores)
     t0 = time.perf_counter()
-    op.oracle_step(orc, h, 0, probe)
+    run_oracle_rows(op.oracle_step, orc, h, 0, probe, cores)
     per_row = (time.perf_counter() - t0) / probe
     rows = int(max(1, min(w.M, total_budget / max(args.steps + args.warmup, 1) / max(per_row, 1e-9))))
     starts = [(i * rows) % max(1, w.M - rows + 1) for i in range(args.steps + args.warmup)]
     for i in range(args.warmup):
-        op.oracle_step(orc, h, starts[i], rows)
+        run_oracle_rows(op.oracle_step, orc, h, starts[i], rows, cores)
     t0 = time.perf_counter()
     for i in range(args.warmup, args.warmup + args.steps):
-        op.oracle_step(orc, h, starts[i], rows)
+        run_oracle_rows(op.oracle_step, orc, h, starts[i], rows, cores)
     dt = time.perf_counter() - t0
     value = op.step_bytes(rows) * args.steps / dt / 1e9
-    sample = f"{rows} consecutive rows of the {w.M}x{w.N} workload per step"
+    sample = (f"{rows} consecutive rows of the {w.M}x{w.N} workload per step, "
+              f"split over {cores} threads")
     line = {
         "impl": "reference", "metric": metric_for(w), "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -365,14 +424,70 @@ def l2_flush(buf):
     buf.view(torch.int32).sum()
 
 
+def needs_flush(w) -> bool:
+    """Workloads whose tensors are under 256 MB each flush the L2 between timed
+    passes; larger ones stream more than the L2 holds anyway."""
+    return w.M * w.N * w.elem_bytes < 256e6
+
+
 def workload_config(w):
     title = "LayerNorm" if w.op == "layernorm" else "RMSNorm"
     return {"workload": f"{title} fwd+bwd {w.dtype} M={w.M} N={w.N} eps={w.eps:g}"
                         + (" offset" if w.offset else ""),
             "name": w.name, "M": w.M, "N": w.N, "io_dtype": w.dtype, "offset": w.offset,
-            "l2": "inputs larger than L2 (no flush)" if w.M * w.N * w.elem_bytes > 129e6
-            else "L2 flushed between steps (512 MB written then read, outside the events)",
+            "l2": "L2 flushed before each pass (512 MB written then read, outside the events)"
+            if needs_flush(w) else "inputs larger than L2 (no flush)",
             "parallelism": "replicas"}
+
+
+def protocol_median_us(fn, stream, flush=None, warmup_calls=20, samples=50, calls=20):
+    """The pages' timing protocol for one pass: warm-up calls, then `samples`
+    samples of `calls` back-to-back calls each, bracketed by CUDA events on the
+    launching stream; returns the median over samples of the per-call time (us).
+    With `flush`, the L2 is flushed before each sample, outside the events."""
+    import torch
+    for _ in range(warmup_calls):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(samples)]
+    for a, b in ev:
+        if flush is not None:
+            l2_flush(flush)
+        a.record(stream)
+        for _ in range(calls):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 / calls for a, b in ev)
+
+
+def link_copy_seconds(pairs_in, pairs_out, dev, reps=3):
+    """Plain pinned-memory copies of one step's bytes, host to device on one
+    stream and device to host on another at the same time (the link is full
+    duplex); the best of `reps`. pairs_in: (device dst, host src); pairs_out:
+    (host dst, device src)."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = None
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        e0.record(cur)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        with torch.cuda.stream(s_in):
+            for d, h in pairs_in:
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in pairs_out:
+                h.copy_(d, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        best = t if best is None else min(best, t)
+    return best
 
 
 # --------------------------------------------------------------------------- #
@@ -411,7 +526,7 @@ def run_ours(args, w):
 
     bufs = device_set()
     flush = None
-    if M * N * w.elem_bytes < 256e6:
+    if needs_flush(w):
         flush = torch.empty(int(512e6), dtype=torch.uint8, device=dev)
 
     def fwd():
@@ -433,7 +548,11 @@ def run_ours(args, w):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # events per step: fwd start, fwd end, bwd start, bwd end. Workloads that fit
+    # in L2 flush it before each pass, outside the events, so that every pass
+    # starts from a clean L2 (the convention of ncu's cache control); the larger
+    # ones run back to back (bwd start = fwd end).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(local, clock_log_path(args, rank))
     time.sleep(0.3)
     barrier(world)
@@ -444,17 +563,25 @@ def run_ours(args, w):
         ev[k][0].record(stream)
         fwd()
         ev[k][1].record(stream)
-        bwd()
+        if flush is not None:
+            l2_flush(flush)
         ev[k][2].record(stream)
+        bwd()
+        ev[k][3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    # the pages' protocol per pass (after the timed region; not part of `value`)
+    proto = None
+    if not args.no_protocol:
+        proto = {"fwd_us_median": protocol_median_us(fwd, stream, flush),
+                 "bwd_us_median": protocol_median_us(bwd, stream, flush)}
     clocks.stop()
-    if flush is None:
-        total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    else:
-        total_ms = sum(ev[k][0].elapsed_time(ev[k][2]) for k in range(K))
     fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    bwd_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
+    if flush is None:
+        total_ms = ev[0][0].elapsed_time(ev[K - 1][3])
+    else:
+        total_ms = sum(fwd_ms) + sum(bwd_ms)
     dev_err = B.rmsnorm_device_error(clear=True)
 
     secs = max_over_ranks(total_ms / 1e3, world, device=dev)
@@ -467,9 +594,11 @@ def run_ours(args, w):
     # other's kernels and copies in the opposite direction (NVLink-C2C is full
     # duplex); the timed region covers all steps on both streams.
     e2e_steps = max(3, min(K, args.e2e_steps))
-    streams = [stream, torch.cuda.Stream(dev)]
-    sets = [bufs, device_set()]
     out_names = [k for k in op.outputs]
+    if args.no_e2e:
+        e2e_steps = 0
+    streams = [stream, torch.cuda.Stream(dev)]
+    sets = [bufs, device_set() if e2e_steps else None]
     houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in out_names}
              for _ in range(2)]
 
@@ -484,22 +613,29 @@ def run_ours(args, w):
             for name in out_names:
                 ho[name].copy_(b[name].view(-1), non_blocking=True)
 
-    e2e_step(0)
-    e2e_step(1)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(streams[0])
-    streams[1].wait_event(e0)
-    for k in range(e2e_steps):
-        e2e_step(k)
-    streams[0].wait_stream(streams[1])
-    e1.record(streams[0])
-    torch.cuda.synchronize()
-    e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
+    e2e_secs = None
+    if e2e_steps:
+        e2e_step(0)
+        e2e_step(1)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(streams[0])
+        streams[1].wait_event(e0)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        streams[0].wait_stream(streams[1])
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in op.inputs)
     d2h = sum(bufs[k].numel() * bufs[k].element_size() for k in out_names)
+    link_s = None
+    if e2e_steps:
+        # the host link alone: the same bytes as one step's copies, no kernels
+        link_s = link_copy_seconds([(bufs[k], host[k]) for k in op.inputs],
+                                   [(houts[0][k], bufs[k].view(-1)) for k in out_names], dev)
 
     if rank != 0:
         return 0
@@ -508,6 +644,31 @@ def run_ours(args, w):
     fwd_avg_ms = statistics.mean(fwd_ms)
     bwd_gbs = w.bwd_bytes() / (bwd_avg_ms / 1e3) / 1e9
     fwd_gbs = w.fwd_bytes() / (fwd_avg_ms / 1e3) / 1e9
+
+    def pass_entry(nbytes, times_ms, pass_id):
+        mean_ms = statistics.mean(times_ms)
+        med_ms = statistics.median(times_ms)
+        gbs = nbytes / (mean_ms / 1e3) / 1e9
+        return {"us": mean_ms * 1e3, "us_median": med_ms * 1e3, "gbs": gbs,
+                "gbs_median": nbytes / (med_ms / 1e3) / 1e9, "frac_of_peak": gbs / peak,
+                "frac_of_nominal_peak": gbs / NOMINAL_HBM_GBS, "bytes": nbytes,
+                "plan": B.rmsnorm_describe_plan(pass_id, M, N, dt)}
+
+    e2e = None
+    if e2e_steps:
+        e2e_value = step_bytes * e2e_steps / e2e_secs / 1e9 * world
+        ceiling = step_bytes / link_s / 1e9
+        e2e = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "link_gbs": (h2d + d2h) / link_s / 1e9,
+               "link_ceiling": ceiling, "frac_of_link_ceiling": e2e_value / world / ceiling,
+               "link_note": "link_gbs: one step's h2d and d2h bytes copied at once (pinned, both directions, "
+                            "no kernels), best of 3; link_ceiling: the e2e value those copies alone allow"}
+    if proto is not None:
+        proto.update({"fwd_gbs": w.fwd_bytes() / proto["fwd_us_median"] / 1e3,
+                      "bwd_gbs": w.bwd_bytes() / proto["bwd_us_median"] / 1e3,
+                      "warmup_calls": 20, "samples": 50, "calls_per_sample": 20,
+                      "l2": "flushed before each sample" if flush is not None
+                      else "inputs larger than L2"})
     p_fwd, p_bwd = op.passes
     traffic = recorded_traffic(f"{op.name}_bwd {w.name}", plan=B.rmsnorm_describe_plan(p_bwd, M, N, dt))
     line = {
@@ -517,25 +678,22 @@ def run_ours(args, w):
         {"bfloat16": "bf16", "float16": "f16"}[dt],
         "data": "synthetic (seeded; see rmsnorm_fwd_bwd_gb300/inputs.py)",
         "config": workload_config(w),
-        "fwd": {"us": fwd_avg_ms * 1e3, "gbs": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
-                "bytes": w.fwd_bytes(), "plan": B.rmsnorm_describe_plan(p_fwd, M, N, dt)},
-        "bwd": {"us": bwd_avg_ms * 1e3, "gbs": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
-                "bytes": w.bwd_bytes(), "plan": B.rmsnorm_describe_plan(p_bwd, M, N, dt)},
+        "fwd": pass_entry(w.fwd_bytes(), fwd_ms, p_fwd),
+        "bwd": pass_entry(w.bwd_bytes(), bwd_ms, p_bwd),
         "roofline": {"bound": "hbm", "kernel": op.kernel,
                      "achieved": bwd_gbs, "peak": peak, "peak_kind": f"{peak_kind} HBM copy",
                      "unit": "GB/s", "frac": bwd_gbs / peak, "traffic": traffic,
-                     "algorithmic_bytes": w.bwd_bytes()},
-        "e2e": {"value": step_bytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                     "algorithmic_bytes": w.bwd_bytes(), "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal_peak": bwd_gbs / NOMINAL_HBM_GBS,
+                     "target": ">= 0.85 of the nominal peak (frac_of_nominal_peak); frac is of the measured copy"},
+        "protocol": proto,
+        "e2e": e2e,
         "gpu_launches": 3 * K,
         "device_error_word": dev_err,
         "clocks": clocks.summary(0, 0),
     }
     if not args.no_cpu_baseline:
-        rate, rows, t = cpu_oracle_rate(w, h_np, args.cpu_budget)
-        line["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"first {rows} rows of the workload, fwd+bwd reference, "
-                                          f"{t:.1f} s"}
+        line["cpu_baseline"] = cpu_baseline(w, h_np, args.cpu_budget)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -577,7 +735,7 @@ def run_double_backward(args, w):
 
     bufs = device_set()
     flush = None
-    if M * N * s < 256e6:
+    if needs_flush(w):
         flush = torch.empty(int(512e6), dtype=torch.uint8, device=dev)
     B.rmsnorm_device_error(clear=True)
     for _ in range(args.warmup):
@@ -687,8 +845,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="workload name (default: the headline)")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--cpu-budget", type=float, default=24.0,
+                    help="seconds of oracle work (three legs: all cores, one thread, fp64 golden)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-protocol", action="store_true",
+                    help="skip the per-pass medians of the pages' protocol (20 warm-up calls, 50 samples x 20)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (one device set only; for profiler captures)")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the raw nvidia-smi clock samples (default: the temporary directory)")
     ap.add_argument("--double-backward", action="store_true",
