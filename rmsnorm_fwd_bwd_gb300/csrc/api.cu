@@ -274,6 +274,12 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     } else {
         if (!bps) {
             bps = static_cast<int>(std::min<int64_t>(std::max<int64_t>(kRingPerSm[pass] / (2 * stage), 1), 4));
+            // few rows per SM: the ring never reaches its steady state and the
+            // tail weighs more, so as many blocks as fit, up to 4 (ncu, L2 clean
+            // before each kernel: bf16 8192x5120 backward row kernel 42.0 -> 35.7
+            // us with 3 blocks of 2 stages instead of 2; bf16 4096x4096 19.3 ->
+            // 18.1 us with 4 instead of 3; measured for the RMSNorm backward only)
+            if (pass == 1 && M <= 64 * static_cast<int64_t>(di.sms)) bps = 4;
             // blocks that fit by registers alone: the ring depth is sized for those
             int fit = 0;
             p.smem = static_cast<size_t>(stage + 8) + fixed;

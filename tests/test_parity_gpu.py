@@ -258,6 +258,15 @@ def test_plan_dispatch():
     assert B.rmsnorm_describe_plan(1, 8192, 4096, "bfloat16", aligned16=2).startswith("scalar")
     assert B.rmsnorm_describe_plan(0, 64, 16383, "float32", aligned16=False).startswith("scalar")
 
+    def blocks_per_sm(plan):
+        f = dict(kv.split("=") for kv in plan.split()[1:])
+        return int(f["units"]) / int(f["sms"])
+    # backward with few rows per SM: as many blocks as fit, up to 4 (smem caps
+    # 20 KB rows at 3); many rows per SM: the 96 KB ring target (3 at 8 KB rows)
+    assert blocks_per_sm(B.rmsnorm_describe_plan(1, 4096, 4096, "bfloat16")) == 4
+    assert blocks_per_sm(B.rmsnorm_describe_plan(1, 8192, 5120, "bfloat16")) == 3
+    assert blocks_per_sm(B.rmsnorm_describe_plan(1, 65536, 4096, "bfloat16")) == 3
+
 
 def test_torch_conveniences_match_raw_calls():
     import torch
