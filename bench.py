@@ -12,8 +12,10 @@ value  = algorithmic bytes of all ranks' steps / max-over-ranks time, in GB/s,
          where fwd bytes = 2*M*N*s + N*s + 4*M and bwd bytes = 3*M*N*s + 2*N*s + 4*M.
 e2e    = the same metric through the C ABI with host buffers: each step copies
          x, gamma, dy from pinned host memory, runs both passes, and copies
-         y, rstd, dx, dgamma back (two streams take alternate steps so copies in
-         both directions overlap kernels).
+         y, rstd, dx, dgamma back; copies in, kernels and copies out run as a
+         pipeline on three streams over two buffer sets, so the two directions
+         of the host link overlap. link_gbs / link_ceiling: plain copies of one
+         step's bytes in both directions at once, timed in the same run.
 roofline = the backward pass (the dominant cost) against the measured HBM copy
          bandwidth in MEASURED_PEAKS.json.
 cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
@@ -490,6 +492,57 @@ def link_copy_seconds(pairs_in, pairs_out, dev, reps=3):
     return best
 
 
+def pipelined_e2e_seconds(steps, sets, houts, copy_in, compute, copy_out, compute_stream, dev):
+    """End-to-end timing of `steps` steps through the public API with host
+    buffers, as a three-stage pipeline on three streams: step k's host-to-device
+    copies (copy_in), its kernels (compute, on compute_stream) and its
+    device-to-host copies (copy_out) use buffer set k % 2, so the copies in of
+    step k + 1 overlap the kernels and the copies out of step k (the host link
+    is full duplex). Events order each stage after the one before it in the
+    same step and after the stage of step k - 2 that last used the same set.
+    Returns the seconds from the first copy in to the last copy out."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_k = compute_stream
+
+    def ev():
+        return torch.cuda.Event()
+
+    def run(n):
+        done_in, done_k, done_out = [], [], []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_k)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for k in range(n):
+            b, ho = sets[k % 2], houts[k % 2]
+            if k >= 2:
+                s_in.wait_event(done_k[k - 2])      # the set's inputs were consumed by step k - 2
+            with torch.cuda.stream(s_in):
+                copy_in(b, s_in)
+            done_in.append(ev())
+            done_in[k].record(s_in)
+            s_k.wait_event(done_in[k])
+            if k >= 2:
+                s_k.wait_event(done_out[k - 2])     # the set's outputs were copied out by step k - 2
+            compute(b, s_k)
+            done_k.append(ev())
+            done_k[k].record(s_k)
+            s_out.wait_event(done_k[k])
+            with torch.cuda.stream(s_out):
+                copy_out(b, ho, s_out)
+            done_out.append(ev())
+            done_out[k].record(s_out)
+        s_k.wait_stream(s_in)
+        s_k.wait_stream(s_out)
+        e1.record(s_k)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    run(2)  # warm-up: both sets touched once
+    return run(steps)
+
+
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
@@ -589,46 +642,32 @@ def run_ours(args, w):
     value = aggregate(step_bytes, K, world, secs)
 
     # end to end through the C ABI with host buffers: every step copies its inputs
-    # in from pinned host memory and its results back out. Two streams with their
-    # own device buffers take alternate steps, so one step's copies overlap the
-    # other's kernels and copies in the opposite direction (NVLink-C2C is full
-    # duplex); the timed region covers all steps on both streams.
-    e2e_steps = max(3, min(K, args.e2e_steps))
+    # in from pinned host memory and its results back out, pipelined over two
+    # buffer sets (pipelined_e2e_seconds)
+    e2e_steps = 0 if args.no_e2e else max(3, min(K, args.e2e_steps))
     out_names = [k for k in op.outputs]
-    if args.no_e2e:
-        e2e_steps = 0
-    streams = [stream, torch.cuda.Stream(dev)]
-    sets = [bufs, device_set() if e2e_steps else None]
-    houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in out_names}
-             for _ in range(2)]
+    sets = [bufs, device_set()] if e2e_steps else None
+    houts = ([{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in out_names}
+              for _ in range(2)] if e2e_steps else None)
 
-    def e2e_step(k):
-        s, b, ho = streams[k % 2], sets[k % 2], houts[k % 2]
-        with torch.cuda.stream(s):
-            for name in op.inputs:
-                b[name].copy_(host[name], non_blocking=True)
-            st = op.fwd(B, b, s) or op.bwd(B, b, s, wsz)
-            if st:
-                raise B.RMSNormError(st, "end-to-end step")
-            for name in out_names:
-                ho[name].copy_(b[name].view(-1), non_blocking=True)
+    def copy_in(b, s):
+        for name in op.inputs:
+            b[name].copy_(host[name], non_blocking=True)
+
+    def compute(b, s):
+        st = op.fwd(B, b, s) or op.bwd(B, b, s, wsz)
+        if st:
+            raise B.RMSNormError(st, "end-to-end step")
+
+    def copy_out(b, ho, s):
+        for name in out_names:
+            ho[name].copy_(b[name].view(-1), non_blocking=True)
 
     e2e_secs = None
     if e2e_steps:
-        e2e_step(0)
-        e2e_step(1)
-        torch.cuda.synchronize()
         barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(streams[0])
-        streams[1].wait_event(e0)
-        for k in range(e2e_steps):
-            e2e_step(k)
-        streams[0].wait_stream(streams[1])
-        e1.record(streams[0])
-        torch.cuda.synchronize()
-        e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
+        e2e_secs = max_over_ranks(pipelined_e2e_seconds(e2e_steps, sets, houts, copy_in, compute, copy_out,
+                                                        stream, dev), world, device=dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in op.inputs)
     d2h = sum(bufs[k].numel() * bufs[k].element_size() for k in out_names)
     link_s = None
@@ -771,40 +810,30 @@ def run_double_backward(args, w):
     value = aggregate(nbytes, K, world, secs)
 
     # end to end with host buffers: each step copies ddx, ddgamma, dy, x, gamma and
-    # rstd in and d_dy, d_x, d_gamma out; two streams alternate as in the main bench
+    # rstd in and d_dy, d_x, d_gamma out, pipelined as in the main bench
     e2e_steps = max(3, min(K, args.e2e_steps))
-    streams = [stream, torch.cuda.Stream(dev)]
     sets = [bufs, device_set()]
     r_host = bufs["r"].cpu().pin_memory()
     houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in ("d_dy", "d_x", "d_g")}
              for _ in range(2)]
 
-    def e2e_step(k):
-        strm, b, ho = streams[k % 2], sets[k % 2], houts[k % 2]
-        with torch.cuda.stream(strm):
-            for name in ("ddx", "ddg", "dy", "x", "g"):
-                b[name].copy_(host[name], non_blocking=True)
-            b["r"].copy_(r_host, non_blocking=True)
-            st = step(b, strm)
-            if st:
-                raise B.RMSNormError(st, "end-to-end double backward")
-            for name in ("d_dy", "d_x", "d_g"):
-                ho[name].copy_(b[name].view(-1), non_blocking=True)
+    def copy_in(b, strm):
+        for name in ("ddx", "ddg", "dy", "x", "g"):
+            b[name].copy_(host[name], non_blocking=True)
+        b["r"].copy_(r_host, non_blocking=True)
 
-    e2e_step(0)
-    e2e_step(1)
-    torch.cuda.synchronize()
+    def compute(b, strm):
+        st = step(b, strm)
+        if st:
+            raise B.RMSNormError(st, "end-to-end double backward")
+
+    def copy_out(b, ho, strm):
+        for name in ("d_dy", "d_x", "d_g"):
+            ho[name].copy_(b[name].view(-1), non_blocking=True)
+
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(streams[0])
-    streams[1].wait_event(e0)
-    for k in range(e2e_steps):
-        e2e_step(k)
-    streams[0].wait_stream(streams[1])
-    e1.record(streams[0])
-    torch.cuda.synchronize()
-    e2e_secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device=dev)
+    e2e_secs = max_over_ranks(pipelined_e2e_seconds(e2e_steps, sets, houts, copy_in, compute, copy_out, stream,
+                                                    dev), world, device=dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in host) + 4 * M
     d2h = 2 * M * N * s + N * s
     if rank != 0:

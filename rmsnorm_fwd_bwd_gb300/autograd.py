@@ -29,12 +29,39 @@ library's kernels at both orders. ``CALLS["double_backward"]`` counts them.
 """
 from __future__ import annotations
 
+import os
+
 import torch
 
 from . import binding
 
 CALLS = {"forward": 0, "backward": 0, "double_backward": 0}
 LN_CALLS = {"forward": 0, "backward": 0}
+
+# A kernel whose bounded wait gives up returns early with its outputs partly
+# unwritten and reports it only through the device error word (the host call
+# itself succeeded). RMSNORM_CHECK_DEVICE_ERROR=1 reads that word after every op
+# (a device synchronisation each time) and raises; otherwise call
+# check_device_error() at the end of a training step.
+CHECK_EVERY_OP = os.environ.get("RMSNORM_CHECK_DEVICE_ERROR", "0") not in ("", "0")
+
+
+class DeviceError(RuntimeError):
+    """A kernel reported a failure through the device error word."""
+
+
+def check_device_error(clear: bool = True) -> None:
+    """Raise DeviceError if any kernel on the current device has set the device
+    error word since it was last cleared (bit 0: a bounded wait gave up; bit 1,
+    debug builds: a read outside its tensor). Synchronizes the device."""
+    word = binding.rmsnorm_device_error(clear=clear)
+    if word:
+        raise DeviceError(f"RMSNorm kernels reported device error word {word:#x}")
+
+
+def _after_op():
+    if CHECK_EVERY_OP:
+        check_device_error()
 
 
 def _rows(x: torch.Tensor):
@@ -62,6 +89,7 @@ def _fwd(x: torch.Tensor, weight: torch.Tensor, eps: float, offset: bool) -> tup
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "rmsnorm_fwd")
     CALLS["forward"] += 1
+    _after_op()
     return y, rstd
 
 
@@ -85,6 +113,7 @@ def _bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, rstd: torch.Te
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "rmsnorm_bwd")
     CALLS["backward"] += 1
+    _after_op()
     return dx, dw
 
 
@@ -128,6 +157,7 @@ def _bwd_bwd(ddx: torch.Tensor, ddw: torch.Tensor, dy: torch.Tensor, x: torch.Te
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "rmsnorm_bwd_bwd")
     CALLS["double_backward"] += 1
+    _after_op()
     return d_dy, d_x, d_w
 
 
@@ -198,6 +228,7 @@ def _ln_fwd(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor,
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "layernorm_fwd")
     LN_CALLS["forward"] += 1
+    _after_op()
     return y, mean, rstd
 
 
@@ -223,6 +254,7 @@ def _ln_bwd(dy: torch.Tensor, x: torch.Tensor, weight: torch.Tensor, mean: torch
     if st != binding.RMSNORM_OK:
         raise binding.RMSNormError(st, "layernorm_bwd")
     LN_CALLS["backward"] += 1
+    _after_op()
     return dx, dw, db
 
 

@@ -33,3 +33,28 @@ def test_bounded_wait_reports_instead_of_hanging():
     res = check.gate_outputs(x, g, dy, "bfloat16", False, 1e-6, y=y, rstd=r, dx=dx, dgamma=dg)
     assert gate.overall(res) == "PASS", gate.report("after timeout", res)
     assert B.rmsnorm_device_error() == 0
+
+
+def test_autograd_surfaces_the_device_error_word(monkeypatch):
+    """The torch ops succeed on the host even when a kernel gave up a bounded
+    wait; check_device_error (or RMSNORM_CHECK_DEVICE_ERROR=1, every op) turns
+    the device error word into an exception. The word is set by the diagnostic
+    wait kernel, never by a fault."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rmsnorm_fwd_bwd_gb300 import autograd as ag
+    B.rmsnorm_device_error(clear=True)
+    x = torch.randn(16, 512, device="cuda", dtype=torch.bfloat16)
+    w = torch.ones(512, device="cuda", dtype=torch.bfloat16)
+    ag.rms_norm(x, w)
+    ag.check_device_error()                                   # clean: no exception
+    assert B.rmsnorm_selftest_wait_timeout(4096) == B.RMSNORM_OK
+    with pytest.raises(ag.DeviceError):
+        ag.check_device_error()
+    ag.check_device_error()                                   # the check cleared the word
+    monkeypatch.setattr(ag, "CHECK_EVERY_OP", True)
+    assert B.rmsnorm_selftest_wait_timeout(4096) == B.RMSNORM_OK
+    with pytest.raises(ag.DeviceError):
+        ag.rms_norm(x, w)
+    assert B.rmsnorm_device_error(clear=True) == 0

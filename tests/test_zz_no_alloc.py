@@ -79,3 +79,36 @@ def test_static_scratch_rejects_bad_arguments_without_launching(torch):
     assert B.rmsnorm_bwd_static_scratch(None, None, g, None, None, dg, 4, 16385, "float32", 0) == 2
     torch.cuda.synchronize()
     assert torch.all(dg == 5.0)
+
+
+def test_static_scratch_call_allocates_nothing(torch):
+    """The defining property: a call takes no device memory. A warm-up call of
+    another shape loads the library's array (with lazy module loading, the
+    first use of the array's module places it on the device), and the shape's
+    kernels are loaded through rmsnorm_bwd (a kernel's first launch may load its
+    code); then the device's free memory is read around the first static-scratch
+    calls of the shape and must not move. (Shapes too large for the array are
+    rejected by the same workspace check rmsnorm_bwd applies, exercised with a
+    short workspace in test_parity_gpu.py: on a 152-SM GB300 every legal shape
+    fits in the 16 MiB.)"""
+    wx, wg, wdy = inputs.make_inputs(64, 1024, "bfloat16", seed=3)
+    _backward_both_ways(torch, wx, wg, wdy, "bfloat16", False)
+    dtype, M, N, offset = "float32", 300, 8192, True
+    x_np, g_np, dy_np = inputs.make_inputs(M, N, dtype, seed=11, offset=offset)
+    x, g, dy = (B.to_device(a.reshape(-1), dtype) for a in (x_np, g_np, dy_np))
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device="cuda")
+    dg = torch.empty_like(g)
+    need = B.rmsnorm_bwd_workspace_size(M, N, dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert B.rmsnorm_fwd(x, g, y, rstd, M, N, 1e-6, dtype, int(offset)) == B.RMSNORM_OK
+    assert B.rmsnorm_bwd(dy, x, g, rstd, dx, dg, M, N, dtype, int(offset), ws, need) == B.RMSNORM_OK
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    torch_before = torch.cuda.memory_allocated()
+    for _ in range(2):
+        assert B.rmsnorm_bwd_static_scratch(dy, x, g, rstd, dx, dg, M, N, dtype, int(offset)) == B.RMSNORM_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert torch.cuda.memory_allocated() == torch_before
+    assert B.rmsnorm_device_error(clear=True) == 0
