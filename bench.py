@@ -811,11 +811,11 @@ def run_double_backward(args, w):
 
     # end to end with host buffers: each step copies ddx, ddgamma, dy, x, gamma and
     # rstd in and d_dy, d_x, d_gamma out, pipelined as in the main bench
-    e2e_steps = max(3, min(K, args.e2e_steps))
-    sets = [bufs, device_set()]
+    e2e_steps = 0 if args.no_e2e else max(3, min(K, args.e2e_steps))
+    sets = [bufs, device_set()] if e2e_steps else None
     r_host = bufs["r"].cpu().pin_memory()
-    houts = [{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in ("d_dy", "d_x", "d_g")}
-             for _ in range(2)]
+    houts = ([{k: torch.empty(bufs[k].numel(), dtype=bufs[k].dtype).pin_memory() for k in ("d_dy", "d_x", "d_g")}
+              for _ in range(2)] if e2e_steps else None)
 
     def copy_in(b, strm):
         for name in ("ddx", "ddg", "dy", "x", "g"):
@@ -831,9 +831,11 @@ def run_double_backward(args, w):
         for name in ("d_dy", "d_x", "d_g"):
             ho[name].copy_(b[name].view(-1), non_blocking=True)
 
-    barrier(world)
-    e2e_secs = max_over_ranks(pipelined_e2e_seconds(e2e_steps, sets, houts, copy_in, compute, copy_out, stream,
-                                                    dev), world, device=dev)
+    e2e_secs = None
+    if e2e_steps:
+        barrier(world)
+        e2e_secs = max_over_ranks(pipelined_e2e_seconds(e2e_steps, sets, houts, copy_in, compute, copy_out,
+                                                        stream, dev), world, device=dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in host) + 4 * M
     d2h = 2 * M * N * s + N * s
     if rank != 0:
@@ -856,8 +858,9 @@ def run_double_backward(args, w):
                      "frac": gbs / peak, "traffic": recorded_traffic(f"rmsnorm_bwd_bwd {w.name}",
                                                                 plan=B.rmsnorm_describe_plan(4, M, N, dt)),
                      "algorithmic_bytes": nbytes},
-        "e2e": {"value": nbytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e": ({"value": nbytes * e2e_steps / e2e_secs / 1e9 * world, "unit": "GB/s",
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+                if e2e_steps else None),
         "gpu_launches": 2 * K,
         "device_error_word": dev_err,
         "clocks": clocks.summary(0, 0),
