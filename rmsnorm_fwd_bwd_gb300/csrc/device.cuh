@@ -107,6 +107,53 @@ template <> struct Elem<kBF16> {
 };
 
 // ---------------------------------------------------------------------------
+// packed fp32 pairs: two lanes in one 64-bit register, one instruction for both
+// (the f32x2 arithmetic of sm_100 and later). Each lane is rounded exactly as
+// the scalar operation (fma.rn / mul.rn / add.rn per lane), so results are the
+// same bits as the scalar code they replace; only the instruction count drops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {  // a * b + c, rounded once
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// y = (x * r) * g, or with the offset variant (g * x) * r where g = 1 + w (added
+// here when add_one, i.e. when w arrives raw), two elements per packed
+// instruction; per element the same two rounded products as the scalar form.
+template <int VEC, bool OFFSET>
+__device__ __forceinline__ void scale_pairs(const float (&x)[VEC], const float (&w)[VEC], bool add_one, float r,
+                                            float (&o)[VEC]) {
+    const uint64_t r2 = f2_pack(r, r);
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) {
+        const uint64_t x2 = f2_pack(x[e], x[e + 1]);
+        uint64_t g2 = f2_pack(w[e], w[e + 1]);
+        if (add_one) g2 = f2_add(f2_pack(1.0f, 1.0f), g2);
+        const uint64_t y2 = OFFSET ? f2_mul(f2_mul(g2, x2), r2) : f2_mul(f2_mul(x2, r2), g2);
+        f2_unpack(y2, o[e], o[e + 1]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // reductions
 // ---------------------------------------------------------------------------
 // Butterfly sum over the 32 lanes. Every lane ends with the same bits: at each

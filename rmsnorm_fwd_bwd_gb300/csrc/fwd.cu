@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
         // x slice widened to fp32 once (or kept raw, see PACK); sum of squares on the way
         float xf[PACK ? 1 : VPT][VEC];
         uint4 xr[PACK ? VPT : 1];
-        float ss0 = 0.f, ss1 = 0.f;
+        // two sums of squares, even and odd elements, as the two lanes of one
+        // packed register
+        uint64_t ss = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
@@ -136,10 +138,12 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
             E::unpack(raw, *reinterpret_cast<float(*)[VEC]>(xv));
 #pragma unroll
             for (int e = 0; e < VEC; e += 2) {
-                ss0 = fmaf(xv[e], xv[e], ss0);
-                ss1 = fmaf(xv[e + 1], xv[e + 1], ss1);
+                const uint64_t x2 = f2_pack(xv[e], xv[e + 1]);
+                ss = f2_fma(x2, x2, ss);
             }
         }
+        float ss0, ss1;
+        f2_unpack(ss, ss0, ss1);
         float* redb = red + (j & 1) * 32;
         const float wsum = warp_allsum(ss0 + ss1);
         if (lane == 0) redb[warp] = wsum;
@@ -191,15 +195,9 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
                         asm volatile("" : "+r"(xw.x), "+r"(xw.y), "+r"(xw.z), "+r"(xw.w));
                         E::unpack(xw, xv);
                         E::unpack(gw, gv);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            const float g = OFFSET ? 1.0f + gv[e] : gv[e];
-                            o[e] = OFFSET ? (g * xv[e]) * r : (xv[e] * r) * g;
-                        }
+                        scale_pairs<VEC, OFFSET>(xv, gv, OFFSET, r, o);
                     } else {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            o[e] = OFFSET ? (gf[v][e] * xf[v][e]) * r : (xf[v][e] * r) * gf[v][e];
+                        scale_pairs<VEC, OFFSET>(xf[v], gf[v], false, r, o);
                     }
                     stg128(yrow + idx * 16, E::pack(o));
                 }

@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (RaggedFwdMinBlocks<DT, VPT>::
             for (int v = 0; v < VPT; ++v) {
                 if (bits[v] == 0u) continue;
                 const int idx = v * nt + tid;
+                // scalar form: the packed one (f32x2) measured slower here (bf16
+                // 8192x4099 forward 29.2 -> 32.6 us), unlike the ring forward
                 float out[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
@@ -239,14 +241,24 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
 #pragma unroll
         for (int q = 0; q < VEC; q += 4) gsm4[(q / 4) * nslot + idx] = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
     }
+    // 2-byte types with up to three vectors per thread run the arithmetic on
+    // packed pairs (f32x2: one instruction for two elements, each rounded as the
+    // scalar operation, so the same bits; bf16 8192x4099: 53.8 -> 52.4 us). With
+    // more vectors the packed form needs more registers than the scalar one (bf16
+    // 128 -> 132, fp16 128 -> 200) and would halve the blocks per SM, and for
+    // fp32 ptxas spilled; those instances keep the scalar form.
+    constexpr bool PACKED = VPT <= 3 && DT != kF32;
     unsigned bits[VPT];
     float acc[VPT][VEC];
+    uint64_t acc2[PACKED ? VPT : 1][VEC / 2];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         int c0;
         bits[v] = ragged::slot_bits<DT>(v * nt + tid, nv, o, N, c0);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC / 2; ++e) acc2[PACKED ? v : 0][e] = f2_pack(0.f, 0.f);
     }
     __syncthreads();
 
@@ -270,13 +282,16 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
         const float r = __shfl_sync(0xffffffffu, r_cur, static_cast<int>(j & 31));
         if (!aborted && !mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
 
-        float xf[VPT][VEC], uf[VPT][VEC];
+        float xf[PACKED ? 1 : VPT][VEC], uf[PACKED ? 1 : VPT][VEC];
+        uint64_t x2[PACKED ? VPT : 1][VEC / 2], u2[PACKED ? VPT : 1][VEC / 2];
         float p0 = 0.f, p1 = 0.f;
+        uint64_t p2 = f2_pack(0.f, 0.f);
+        const uint64_t r2 = f2_pack(r, r);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
-            float df[VEC];
-            E::unpack(ragged::slot_load<DT>(st, idx, bits[v]), xf[v]);
+            float xv[VEC], df[VEC];
+            E::unpack(ragged::slot_load<DT>(st, idx, bits[v]), xv);
             E::unpack(ragged::slot_load<DT>(st + stride, idx, bits[v]), df);
             float g[VEC];
             if (bits[v]) {
@@ -289,13 +304,29 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) g[e] = 0.f;
             }
+            if constexpr (PACKED) {
+                // u = dy * g, the row sum of u * x in two lanes (even and odd elements)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                uf[v][e] = __fmul_rn(df[e], g[e]);
-                if (e & 1) p1 = fmaf(uf[v][e], xf[v][e], p1); else p0 = fmaf(uf[v][e], xf[v][e], p0);
-                acc[v][e] = fmaf(__fmul_rn(df[e], xf[v][e]), r, acc[v][e]);
+                for (int e = 0; e < VEC; e += 2) {
+                    const uint64_t xx = f2_pack(xv[e], xv[e + 1]);
+                    const uint64_t dd = f2_pack(df[e], df[e + 1]);
+                    const uint64_t uu = f2_mul(dd, f2_pack(g[e], g[e + 1]));
+                    p2 = f2_fma(uu, xx, p2);
+                    acc2[v][e / 2] = f2_fma(f2_mul(dd, xx), r2, acc2[v][e / 2]);
+                    x2[v][e / 2] = xx;
+                    u2[v][e / 2] = uu;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    xf[v][e] = xv[e];
+                    uf[v][e] = __fmul_rn(df[e], g[e]);
+                    if (e & 1) p1 = fmaf(uf[v][e], xv[e], p1); else p0 = fmaf(uf[v][e], xv[e], p0);
+                    acc[v][e] = fmaf(__fmul_rn(df[e], xv[e]), r, acc[v][e]);
+                }
             }
         }
+        if constexpr (PACKED) f2_unpack(p2, p0, p1);
         float* redb = red + (j & 1) * 32;
         const float wsum = warp_allsum(p0 + p1);
         if (lane == 0) redb[warp] = wsum;
@@ -325,8 +356,16 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
                 if (bits[v] == 0u) continue;
                 const int idx = v * nt + tid;
                 float out[VEC];
+                if constexpr (PACKED) {
+                    // fma(x, -k, r*u) = fma(-x, k, r*u): the product's sign is exact
+                    const uint64_t nk2 = f2_pack(-k, -k);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) out[e] = fmaf(-xf[v][e], k, __fmul_rn(r, uf[v][e]));
+                    for (int e = 0; e < VEC; e += 2)
+                        f2_unpack(f2_fma(x2[v][e / 2], nk2, f2_mul(r2, u2[v][e / 2])), out[e], out[e + 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) out[e] = fmaf(-xf[v][e], k, __fmul_rn(r, uf[v][e]));
+                }
                 if (bits[v] == kAll && same_phase) {
                     stg128(dxrow - o + idx * 16, E::pack(out));
                 } else {
@@ -346,9 +385,19 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
             const int c0 = (16 * idx - o) / E::kBytes;
+            float af[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                if constexpr (PACKED) {
+                    f2_unpack(acc2[v][e / 2], af[e], af[e + 1]);
+                } else {
+                    af[e] = acc[v][e];
+                    af[e + 1] = acc[v][e + 1];
+                }
+            }
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
-                if ((bits[v] >> e) & 1u) wrow[c0 + e] = acc[v][e];
+                if ((bits[v] >> e) & 1u) wrow[c0 + e] = af[e];
         }
     }
     if (aborted && tid == 0) {
