@@ -697,7 +697,7 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     if (!aligned(dgamma, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (M == 0) {
-        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs) != cudaSuccess)
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), workspace_pitch(N), dgamma, cs) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
     }
@@ -716,7 +716,7 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     CallPlan c;
     if ((st = plan_call(1, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
     const Plan& p = c.plan;
-    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
     a.x = x;
@@ -725,6 +725,7 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     a.rstd_in = rstd;
     a.dx = dx;
     a.ws = static_cast<float*>(workspace);
+    a.ldws = workspace_pitch(N);
     a.M = M;
     a.N = static_cast<int>(N);
     a.ldx = ldx;
@@ -733,7 +734,7 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     a.stages = p.stages;
     a.err = c.err;
     if (launch_pass(1, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -788,7 +789,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     if (!aligned(dgamma, s) || !aligned(dbeta, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (M == 0) {
-        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), dgamma, cs, dbeta) != cudaSuccess)
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), workspace_pitch(N), dgamma, cs, dbeta) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
     }
@@ -806,7 +807,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     CallPlan c;
     if ((st = plan_call(3, M, static_cast<int>(N), dtype, 0, layout, c)) != RMSNORM_OK) return st;
     const Plan& p = c.plan;
-    const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
     a.x = x;
@@ -816,6 +817,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     a.rstd_in = rstd;
     a.dx = dx;
     a.ws = static_cast<float*>(workspace);
+    a.ldws = workspace_pitch(N);
     a.M = M;
     a.N = static_cast<int>(N);
     a.ldx = ldx;
@@ -824,7 +826,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     a.stages = p.stages;
     a.err = c.err;
     if (launch_pass(3, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, dgamma, cs, dbeta) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, dgamma, cs, dbeta) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -843,7 +845,7 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     if (!aligned(d_gamma, s)) return RMSNORM_ERR_ALIGN;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (M == 0) {
-        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), d_gamma, cs) != cudaSuccess)
+        if (launch_dgamma_reduce(dtype, nullptr, 0, static_cast<int>(N), workspace_pitch(N), d_gamma, cs) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         return RMSNORM_OK;
     }
@@ -866,7 +868,7 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     CallPlan c;
     if ((st = plan_call(4, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
     const Plan& p = c.plan;
-    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(N) * sizeof(float);
+    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
     if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
     a.x = x;
@@ -878,6 +880,7 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     a.d_dy = d_dy;
     a.dx = d_x;
     a.ws = static_cast<float*>(workspace);
+    a.ldws = workspace_pitch(N);
     a.M = M;
     a.N = static_cast<int>(N);
     a.ldx = ldx;
@@ -888,7 +891,7 @@ rmsnorm_status bwd_bwd_impl(const void* ddx, int64_t ldddx, const void* ddgamma,
     a.stages = p.stages;
     a.err = c.err;
     if (launch_pass(4, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, d_gamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, d_gamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -919,7 +922,7 @@ extern "C" size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype
         for (int off = 0; off < 2; ++off)
             if (get_plan(1, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
                 units = p.units;
-    return static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+    return static_cast<size_t>(units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
 }
 
 extern "C" rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
@@ -954,7 +957,7 @@ extern "C" size_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dty
     Plan p;
     for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
         if (get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p) && p.units > units) units = p.units;
-    return 2 * static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+    return 2 * static_cast<size_t>(units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
 }
 
 extern "C" rmsnorm_status layernorm_bwd(const void* dy, int64_t lddy, const void* x, int64_t ldx, const void* gamma,
@@ -977,7 +980,7 @@ extern "C" size_t rmsnorm_bwd_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_d
         for (int off = 0; off < 2; ++off)
             if (get_plan(4, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
                 units = p.units;
-    return static_cast<size_t>(units) * static_cast<size_t>(N) * sizeof(float);
+    return static_cast<size_t>(units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
 }
 
 extern "C" rmsnorm_status rmsnorm_bwd_bwd(const void* ddx, int64_t ldddx, const void* ddgamma, const void* dy,

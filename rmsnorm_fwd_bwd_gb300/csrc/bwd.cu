@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(BwdTmaBounds<DT, VPT, CLUSTER>::threads, (BwdT
     griddep_launch_dependents();
     // one row of dgamma partials per cluster: ws[cid][crank*ns + ...]
     if (!aborted) {
-        float* wrow = a.ws + static_cast<size_t>(cid) * a.N + static_cast<size_t>(crank) * ns;
+        float* wrow = a.ws + static_cast<size_t>(cid) * a.ldws + static_cast<size_t>(crank) * ns;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
     }
     griddep_launch_dependents();
     if (blockIdx.x < a.M) {
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
         for (int c = tid; c < N; c += nt) wrow[c] = acc[c];
     }
 }
@@ -306,23 +306,24 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 // dgamma[j] = sum_{p < units} ws[p][j] in a fixed order, without atomics.
 // A block owns an 8-column tile (two float4 lanes) of the partial rows and
 // 128 row lanes: lane (cq, rq) of warp w owns columns 4cq..4cq+3 and rows
-// ry = 16w + rq, ry + 128, ... Each thread issues kReduceBatch loads before
-// adding any of them, so a launch keeps the whole workspace in flight: the
-// partial rows were just written and sit in L2, and the kernel is bound by
-// latency, not bandwidth (measured with ncu at 456 partial rows of 4096: 3.8 us
-// against 4.5 us for 32-column tiles split over 4-CTA clusters, and 1.8 us for
-// an empty kernel). The row sums are combined in a fixed tree: in row order
-// within a thread, a butterfly over the 16 row lanes of a warp, then the 8
-// warps in order through shared memory; the result is rounded once into the
-// I/O dtype. The order depends only on (units, N), so dgamma is bitwise
-// reproducible. units == 0 (no rows) writes zeros. Rows of N % 4 != 0 floats
-// are read one column at a time. blockIdx.y = 1 sums the second plane
+// ry = 16w + rq, ry + 128, ... Partial rows are ldws floats apart, ldws a
+// multiple of 4, so every load is a 16-byte float4 (the up to three pad columns
+// after N are read but never stored). Each thread issues kReduceBatch loads
+// before adding any of them, so a launch keeps the whole workspace in flight:
+// the partial rows were just written and sit in L2, and the kernel is bound by
+// latency, not bandwidth (ncu at 456 partial rows of 4096: 3.8 us, against
+// 4.5 us for 32-column tiles split over 4-CTA clusters; an empty kernel takes
+// 1.8 us). The row sums are combined in a fixed tree: in row order within a
+// thread, a butterfly over the 16 row lanes of a warp, then the 8 warps in
+// order through shared memory; the result is rounded once into the I/O dtype.
+// The order depends only on (units, N), so dgamma is bitwise reproducible.
+// units == 0 (no rows) writes zeros. blockIdx.y = 1 sums the second plane
 // (LayerNorm's dbeta partials) into out1.
 constexpr int kReduceBatch = 8;
 constexpr int kReduceLanes = 2;                  // float4 lanes per row: 8 columns
 constexpr int kReduceRows = 256 / kReduceLanes;  // row lanes per block
 template <int DT>
-__global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
+__global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N, int64_t ldws,
                                                            void* out0, void* out1) {
     using E = Elem<DT>;
     __shared__ float4 part[8][kReduceLanes];
@@ -332,43 +333,22 @@ __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int
     const int ry = warp * (32 / kReduceLanes) + lane / kReduceLanes;
     const int col = blockIdx.x * (4 * kReduceLanes) + cq * 4;
     void* dgamma = blockIdx.y == 0 ? out0 : out1;
-    if (blockIdx.y != 0) ws += units * static_cast<int64_t>(N);
+    if (blockIdx.y != 0) ws += units * ldws;
     griddep_wait();  // the partial sums come from the row kernel just before
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if ((N & 3) == 0) {
-        if (col < N) {
-            for (int64_t base = ry; base < units; base += kReduceRows * kReduceBatch) {
-                float4 v[kReduceBatch];
-#pragma unroll
-                for (int i = 0; i < kReduceBatch; ++i) {
-                    const int64_t p = base + kReduceRows * i;
-                    v[i] = p < units ? __ldcg(reinterpret_cast<const float4*>(ws + p * N + col))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int i = 0; i < kReduceBatch; ++i) {
-                    if (base + kReduceRows * i < units) {
-                        s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w;
-                    }
-                }
-            }
-        }
-    } else if (col < N) {
-        // rows of N % 4 != 0 floats are not 16-byte aligned: one column at a
-        // time, still kReduceBatch rows in flight
-        const int nc = N - col < 4 ? N - col : 4;
+    if (col < N) {
         for (int64_t base = ry; base < units; base += kReduceRows * kReduceBatch) {
-            float v[kReduceBatch][4];
+            float4 v[kReduceBatch];
 #pragma unroll
             for (int i = 0; i < kReduceBatch; ++i) {
                 const int64_t p = base + kReduceRows * i;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[i][e] = (p < units && e < nc) ? __ldcg(ws + p * N + col + e) : 0.f;
+                v[i] = p < units ? __ldcg(reinterpret_cast<const float4*>(ws + p * ldws + col))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int i = 0; i < kReduceBatch; ++i) {
                 if (base + kReduceRows * i < units) {
-                    s.x += v[i][0]; s.y += v[i][1]; s.z += v[i][2]; s.w += v[i][3];
+                    s.x += v[i].x; s.y += v[i].y; s.z += v[i].z; s.w += v[i].w;
                 }
             }
         }
@@ -470,7 +450,7 @@ cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStre
     return cudaLaunchKernelExC(&cfg, k, params);
 }
 
-cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
+cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
                                  cudaStream_t s, void* dbeta) {
     const void* k = dgamma_reduce_kernel_ptr(dtype);
     if (!k) return cudaErrorInvalidDeviceFunction;
@@ -484,7 +464,7 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* params[] = {const_cast<float**>(&ws), &units, &N, &dgamma, &dbeta};
+    void* params[] = {const_cast<float**>(&ws), &units, &N, &ldws, &dgamma, &dbeta};
     return cudaLaunchKernelExC(&cfg, k, params);
 }
 

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(DbwdTmaThreads<VPT, CLUSTER>::value) dbwd_tma_
 
     griddep_launch_dependents();
     if (!aborted) {
-        float* wrow = a.ws + static_cast<size_t>(cid) * a.N + static_cast<size_t>(crank) * ns;
+        float* wrow = a.ws + static_cast<size_t>(cid) * a.ldws + static_cast<size_t>(crank) * ns;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kScalarThreads) dbwd_scalar_kernel(const RowAr
     }
     griddep_launch_dependents();
     if (blockIdx.x < a.M) {
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
         for (int col = tid; col < N; col += nt) wrow[col] = acc[col];
     }
 }

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kRaggedDbwdMaxThreads) dbwd_ragged_kernel(cons
     griddep_launch_dependents();
     // one row of d_gamma partials per block (zeros for a block without rows)
     if (!aborted) {
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c0 = (16 * (v * nt + tid) - o) / E::kBytes;

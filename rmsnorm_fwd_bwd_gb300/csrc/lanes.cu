@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kLaneThreads) bwd_lanes_kernel(const RowArgs a
         rq.push(r_nxt);
     }
     griddep_launch_dependents();
-    block_partials<G, KV, VEC>(acc, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * N);
+    block_partials<G, KV, VEC>(acc, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * a.ldws);
 }
 
 // ---------------------------------------------------------------------------
@@ -458,10 +458,10 @@ __global__ void __launch_bounds__(kLaneThreads) ln_bwd_lanes_kernel(const RowArg
     }
     griddep_launch_dependents();
     // plane 0: dgamma partials, plane 1: dbeta partials, one row per block each
-    block_partials<G, KV, VEC>(accg, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * N);
+    block_partials<G, KV, VEC>(accg, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * a.ldws);
     __syncthreads();
     block_partials<G, KV, VEC>(accb, nvec, N, red,
-                               a.ws + (static_cast<size_t>(gridDim.x) + blockIdx.x) * static_cast<size_t>(N));
+                               a.ws + (static_cast<size_t>(gridDim.x) + blockIdx.x) * static_cast<size_t>(a.ldws));
 }
 
 // ---------------------------------------------------------------------------
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kLaneThreads) dbwd_lanes_kernel(const RowArgs 
         rq.push(r_nxt);
     }
     griddep_launch_dependents();
-    block_partials<G, KV, VEC>(acc, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * N);
+    block_partials<G, KV, VEC>(acc, nvec, N, red, a.ws + static_cast<size_t>(blockIdx.x) * a.ldws);
 }
 
 // ---------------------------------------------------------------------------

@@ -17,7 +17,9 @@ struct RowArgs {
     void* y;               // forward output
     float* rstd_out;       // forward output
     void* dx;              // backward output
-    float* ws;             // backward: dgamma partials [units][N] (LayerNorm: then dbeta partials)
+    float* ws;             // backward: dgamma partials [units][ldws] (LayerNorm: then dbeta partials)
+    int64_t ldws;          // floats between partial rows: N rounded up to a multiple of 4, so that
+                           // every partial row starts on a 16-byte boundary
     const void* beta;      // LayerNorm forward
     float* mean_out;       // LayerNorm forward output (may be null, as may rstd_out there)
     const float* mean_in;  // LayerNorm backward: saved mean per row
@@ -95,8 +97,11 @@ const void* dgamma_reduce_kernel_ptr(int dtype);
 // programmatic stream serialization.
 cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s);
 // Column sums of the partial rows: dgamma from plane 0 of ws and, when dbeta is
-// not null, dbeta from plane 1 (planes of units x N floats, one after the other).
-cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, void* dgamma,
+// not null, dbeta from plane 1 (planes of units rows of ldws floats, one after the
+// other; ldws a multiple of 4).
+// Floats between the workspace's partial rows for rows of N elements.
+inline int64_t workspace_pitch(int64_t N) { return (N + 3) / 4 * 4; }
+cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
                                  cudaStream_t s, void* dbeta = nullptr);
 
 // Device address of the error word in the current context (nullptr on failure),

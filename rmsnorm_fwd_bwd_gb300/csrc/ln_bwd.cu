@@ -208,8 +208,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_tma_kernel(const RowArg
     griddep_launch_dependents();
     // one row of dgamma partials (plane 0) and of dbeta partials (plane 1) per cluster
     if (!aborted) {
-        const size_t plane = static_cast<size_t>(ncl) * a.N;
-        float* wrow = a.ws + static_cast<size_t>(cid) * a.N + static_cast<size_t>(crank) * ns;
+        const size_t plane = static_cast<size_t>(ncl) * a.ldws;
+        float* wrow = a.ws + static_cast<size_t>(cid) * a.ldws + static_cast<size_t>(crank) * ns;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(kScalarThreads) ln_bwd_scalar_kernel(const Row
     }
     griddep_launch_dependents();
     if (blockIdx.x < a.M) {
-        const size_t plane = static_cast<size_t>(gridDim.x) * N;
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        const size_t plane = static_cast<size_t>(gridDim.x) * a.ldws;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
         for (int c = tid; c < N; c += nt) {
             wrow[c] = accg[c];
             wrow[plane + c] = accb[c];

@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(kTmaMaxThreads) ln_bwd_ragged_kernel(const Row
     griddep_launch_dependents();
     // one row of dgamma partials (plane 0) and dbeta partials (plane 1) per block
     if (!aborted) {
-        const size_t plane = static_cast<size_t>(gridDim.x) * N;
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        const size_t plane = static_cast<size_t>(gridDim.x) * a.ldws;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c0 = (16 * (v * nt + tid) - o) / E::kBytes;

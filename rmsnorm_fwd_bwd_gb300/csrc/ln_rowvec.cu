@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(kScalarThreads) ln_bwd_rowvec_kernel(const Row
     griddep_launch_dependents();
     // one row of dgamma partials (plane 0) and dbeta partials (plane 1) per block,
     // zeros for a block without rows; the vector slots tile the row
-    const size_t plane = static_cast<size_t>(gridDim.x) * N;
-    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+    const size_t plane = static_cast<size_t>(gridDim.x) * a.ldws;
+    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
         const int idx = tid + k * nt;

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kTmaMaxThreads) bwd_ragged_kernel(const RowArg
     griddep_launch_dependents();
     // one row of dgamma partials per block (zeros for a block without rows)
     if (!aborted) {
-        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+        float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;

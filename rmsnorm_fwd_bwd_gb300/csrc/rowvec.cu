@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_rowvec_kernel(const RowArg
     griddep_launch_dependents();
     // one row of dgamma partials per block (zeros for a block without rows): the
     // vector slots of one phase tile the row, so every column is written once
-    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * N;
+    float* wrow = a.ws + static_cast<size_t>(blockIdx.x) * a.ldws;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
         const int idx = tid + k * nt;
