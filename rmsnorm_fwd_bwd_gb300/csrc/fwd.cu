@@ -126,9 +126,12 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
         // x slice widened to fp32 once (or kept raw, see PACK); sum of squares on the way
         float xf[PACK ? 1 : VPT][VEC];
         uint4 xr[PACK ? VPT : 1];
-        // two sums of squares, even and odd elements, as the two lanes of one
-        // packed register
+        // two sums of squares, even and odd elements: the two lanes of one packed
+        // f32x2 register, except in the 64-element instances (PACK), where the
+        // packed form measured slower (fp16 16384x16384 forward: 175.9 us scalar,
+        // 177.8 packed)
         uint64_t ss = f2_pack(0.f, 0.f);
+        float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int idx = v * nt + tid;
@@ -138,12 +141,16 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
             E::unpack(raw, *reinterpret_cast<float(*)[VEC]>(xv));
 #pragma unroll
             for (int e = 0; e < VEC; e += 2) {
-                const uint64_t x2 = f2_pack(xv[e], xv[e + 1]);
-                ss = f2_fma(x2, x2, ss);
+                if constexpr (PACK) {
+                    ss0 = fmaf(xv[e], xv[e], ss0);
+                    ss1 = fmaf(xv[e + 1], xv[e + 1], ss1);
+                } else {
+                    const uint64_t x2 = f2_pack(xv[e], xv[e + 1]);
+                    ss = f2_fma(x2, x2, ss);
+                }
             }
         }
-        float ss0, ss1;
-        f2_unpack(ss, ss0, ss1);
+        if constexpr (!PACK) f2_unpack(ss, ss0, ss1);
         float* redb = red + (j & 1) * 32;
         const float wsum = warp_allsum(ss0 + ss1);
         if (lane == 0) redb[warp] = wsum;
@@ -195,7 +202,11 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
                         asm volatile("" : "+r"(xw.x), "+r"(xw.y), "+r"(xw.z), "+r"(xw.w));
                         E::unpack(xw, xv);
                         E::unpack(gw, gv);
-                        scale_pairs<VEC, OFFSET>(xv, gv, OFFSET, r, o);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            const float g = OFFSET ? 1.0f + gv[e] : gv[e];
+                            o[e] = OFFSET ? (g * xv[e]) * r : (xv[e] * r) * g;
+                        }
                     } else {
                         scale_pairs<VEC, OFFSET>(xf[v], gf[v], false, r, o);
                     }
