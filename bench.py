@@ -555,6 +555,8 @@ def run_ours(args, w):
     init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
+    if args.static_rows:
+        assert B.rmsnorm_set_row_pool(False) == B.RMSNORM_OK
     op = op_for(w)
     dt = w.dtype
     M, N = w.M, w.N
@@ -716,7 +718,7 @@ def run_ours(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if dt == "float32" else
         {"bfloat16": "bf16", "float16": "f16"}[dt],
         "data": "synthetic (seeded; see rmsnorm_fwd_bwd_gb300/inputs.py)",
-        "config": workload_config(w),
+        "config": dict(workload_config(w), **({"bwd_rows": "static (no row pool)"} if args.static_rows else {})),
         "fwd": pass_entry(w.fwd_bytes(), fwd_ms, p_fwd),
         "bwd": pass_entry(w.bwd_bytes(), bwd_ms, p_bwd),
         "roofline": {"bound": "hbm", "kernel": op.kernel,
@@ -890,6 +892,8 @@ def main(argv=None):
                     help="time the RMSNorm double backward on the workload instead of fwd+bwd")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the row count M (small cases for profiler captures)")
+    ap.add_argument("--static-rows", action="store_true",
+                    help="RMSNorm backward without the row pool (every block keeps a fixed share of the rows)")
     args = ap.parse_args(argv)
     import dataclasses
     from rmsnorm_fwd_bwd_gb300 import inputs

@@ -16,10 +16,12 @@
  *
  * Means divide by the logical N. All arithmetic is fp32 whatever the I/O dtype;
  * inputs are converted at load and each output element is rounded once, to
- * nearest-even, into the I/O dtype. dgamma is deterministic: fp32 partial sums
- * per persistent thread block, then one fixed-order column reduction (no
- * floating-point atomics), so repeated calls on the same device give identical
- * bits.
+ * nearest-even, into the I/O dtype. dgamma is deterministic: fp32 partial sums,
+ * each over a fixed set of rows added in row order, then one fixed-order column
+ * reduction (no floating-point atomics), so repeated calls on the same device
+ * with the same workspace size give identical bits. (The backward hands its last
+ * rows out dynamically, in segments that each have their own partial sum, so
+ * the sums do not depend on which thread block ran which rows.)
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers on the current CUDA device. The
@@ -96,9 +98,12 @@ rmsnorm_status rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rst
 /*
  * Bytes of device workspace rmsnorm_bwd needs for this shape on the CURRENT
  * device (it depends on the device's SM count). The workspace holds float32
- * dgamma partial sums, one row of N per persistent block (or cluster); it must
- * be 16-byte aligned. Returns 0 when M == 0 or when an argument is invalid
- * (rmsnorm_bwd then reports the precise error). Host-only; launches nothing.
+ * dgamma partial sums, rows of N (padded to a multiple of 4 floats): one per
+ * persistent block (or cluster) and, for the plans that hand their last rows out
+ * from a queue, one per queued segment of rows plus the queue's 16 bytes (about
+ * 1170 rows, 18 MiB, for bf16 65536 x 4096 on a 152-SM GB300). It must be 16-byte
+ * aligned. Returns 0 when M == 0 or when an argument is invalid (rmsnorm_bwd then
+ * reports the precise error). Host-only; launches nothing.
  */
 size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype);
 
@@ -108,8 +113,12 @@ size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype dtype);
  * dgamma[N] (dtype). Two launches on `stream`: the fused row kernel (dx and
  * per-block dgamma partials into `workspace`) and the column reduction.
  * `workspace` must hold at least rmsnorm_bwd_workspace_size(M, N, dtype)
- * bytes (it may be NULL when that is 0). The workspace is scratch: its contents
- * on entry are ignored and on return are unspecified.
+ * bytes (it may be NULL when that is 0); a smaller one that still holds one
+ * partial row per block is used without the row queue (every block then keeps a
+ * fixed share of the rows: other partial sums, equally within the error bound,
+ * and slower on large M). The workspace is scratch: its contents on entry are
+ * ignored and on return are unspecified. Calls whose kernels overlap on the GPU
+ * must not share a workspace.
  */
 rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                            const float* rstd, void* dx, void* dgamma,
@@ -127,10 +136,11 @@ rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
  * Same arguments and results as rmsnorm_bwd, minus the workspace: the dgamma
  * partial sums go to a fixed array of RMSNORM_STATIC_SCRATCH_BYTES (16 MiB)
  * inside the library, which every GPU that loads the library holds until the
- * process exits. Shapes whose partial sums need more than that (see
- * rmsnorm_bwd_workspace_size) are rejected with RMSNORM_ERR_WORKSPACE before
- * anything is launched; on a 152-SM GB300 the measured workloads need at most
- * about 10 MiB.
+ * process exits. It is used as a workspace of that size (see rmsnorm_bwd:
+ * without the row queue when the queue's partial rows do not fit); shapes whose
+ * partial sums need more than that even then are rejected with
+ * RMSNORM_ERR_WORKSPACE before anything is launched; on a 152-SM GB300 the
+ * measured workloads need at most about 10 MiB without the queue.
  *
  * Every call looks up the array's device address in the current context (a
  * host-side runtime query, no allocation), so a device reset between calls is
@@ -138,7 +148,9 @@ rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
  * so make that first call before any stream capture. No call allocates. All calls on a device share the one array: two
  * calls whose kernels overlap on the GPU (for example on different streams
  * without ordering between them) race on it and give wrong dgamma. The array
- * keeps the last call's partial sums; nothing in it has to start at zero.
+ * keeps the last call's partial sums and queue word; nothing in it has to start
+ * at zero (a queue word from an earlier call carries that call's ticket and
+ * starts a fresh queue).
  */
 #define RMSNORM_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 rmsnorm_status rmsnorm_bwd_static_scratch(const void* dy, const void* x, const void* gamma,

@@ -67,6 +67,11 @@ def _load():
             "rmsnorm_device_error": (I, [U32P, I]),
             "rmsnorm_describe_plan": (I, [I, I64, I64, I, I, ctypes.c_char_p, SZ]),
             "rmsnorm_set_launch_override": (I, [I, I, I, I, I]),
+            "rmsnorm_set_row_pool": (I, [I]),
+            "rmsnorm_set_row_pool_shape": (I, [I, I, I, I]),
+            "rmsnorm_row_pool_layout": (I, [I64, I64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+            "rmsnorm_row_pool_segment": (I, [I64, I64, I64, ctypes.POINTER(ctypes.c_int64),
+                                             ctypes.POINTER(ctypes.c_int64)]),
             "rmsnorm_bwd_static_scratch": (I, [P, P, P, P, P, P, I64, I64, I, I, P]),
             "rmsnorm_selftest_wait_timeout": (I, [ctypes.c_uint32, P]),
             "rmsnorm_fwd_strided": (I, [P, I64, P, P, I64, P, I64, I64, F, I, I, P]),
@@ -228,6 +233,32 @@ def rmsnorm_describe_plan(pass_, M, N, dtype, aligned16=True) -> str:
 def rmsnorm_set_launch_override(pass_, threads=0, vpt=0, stages=0, blocks_per_sm=0) -> int:
     return _load().rmsnorm_set_launch_override(int(pass_), int(threads), int(vpt), int(stages),
                                                int(blocks_per_sm))
+
+
+def rmsnorm_set_row_pool(enabled: bool) -> int:
+    return _load().rmsnorm_set_row_pool(int(bool(enabled)))
+
+
+def rmsnorm_set_row_pool_shape(head_pct=0, head_pct_few=0, len_max=0, len_min=0) -> int:
+    return _load().rmsnorm_set_row_pool_shape(int(head_pct), int(head_pct_few), int(len_max), int(len_min))
+
+
+def rmsnorm_row_pool_layout(M: int, G: int):
+    """(head rows per CTA, segments in the queue) of the backward's row pool."""
+    head, nseg = ctypes.c_int64(), ctypes.c_int64()
+    st = _load().rmsnorm_row_pool_layout(int(M), int(G), ctypes.byref(head), ctypes.byref(nseg))
+    if st != RMSNORM_OK:
+        raise RMSNormError(st, "rmsnorm_row_pool_layout")
+    return head.value, nseg.value
+
+
+def rmsnorm_row_pool_segment(M: int, G: int, k: int):
+    """Rows [first, last) of segment k of the backward's row pool."""
+    first, last = ctypes.c_int64(), ctypes.c_int64()
+    st = _load().rmsnorm_row_pool_segment(int(M), int(G), int(k), ctypes.byref(first), ctypes.byref(last))
+    if st != RMSNORM_OK:
+        raise RMSNormError(st, "rmsnorm_row_pool_segment")
+    return first.value, last.value
 
 
 # --------------------------------------------------------------------------- #

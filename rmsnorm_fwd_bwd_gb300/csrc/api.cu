@@ -13,11 +13,14 @@
 // rather than routed to another implementation (section "Adapting the kernel
 // and moving to production": no silent fallback).
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <random>
 #include <tuple>
 
 #include "../../include/layernorm.h"
@@ -83,6 +86,8 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 Override g_override[kPasses];
 unsigned g_override_gen = 0;
+bool g_row_pool = true;  // rmsnorm_set_row_pool
+RowPoolShape g_pool_shape;  // rmsnorm_set_row_pool_shape
 std::map<std::tuple<int, int, int64_t, int, int, int, int, unsigned>, Plan> g_plans;
 std::map<std::pair<const void*, int>, bool> g_attr_done;
 
@@ -128,6 +133,20 @@ uint32_t* error_word_address() {
     return static_cast<uint32_t*>(p);
 }
 
+// A ticket per backward call that uses the row pool (the owner of the queue
+// word, see pool_take in bwd.cu): consecutive values of a process-wide 32-bit
+// counter started at a random value, so that calls in a row never share one (a
+// workspace would have to sit unused through 2^32 calls to meet its own ticket
+// again).
+unsigned long long next_call_ticket() {
+    static std::atomic<uint32_t> counter{[] {
+        std::random_device rd;
+        const auto t = std::chrono::steady_clock::now().time_since_epoch().count();
+        return static_cast<uint32_t>(rd()) ^ static_cast<uint32_t>(t) ^ static_cast<uint32_t>(t >> 32);
+    }()};
+    return counter.fetch_add(1u);
+}
+
 // Caller holds g_mu. Allows the largest dynamic shared memory once per kernel and device.
 bool prepare_kernel(const void* k, int dev, const DeviceInfo& di) {
     auto key = std::make_pair(k, dev);
@@ -155,7 +174,8 @@ void forget_kernel_attributes(int dev) {
 bool occupancy_units(const void* k, const Plan& p, const DeviceInfo& di, int cap_per_sm, int64_t& units) {
     if (p.cluster == 1) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, p.threads, p.smem) != cudaSuccess) return false;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, p.threads + p.extra_threads, p.smem) != cudaSuccess)
+            return false;
         if (cap_per_sm > 0 && n > cap_per_sm) n = cap_per_sm;
         if (n < 1) return false;
         units = static_cast<int64_t>(n) * di.sms;
@@ -163,7 +183,7 @@ bool occupancy_units(const void* k, const Plan& p, const DeviceInfo& di, int cap
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * di.sms), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads + p.extra_threads), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -298,6 +318,19 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     int64_t units = 0;
     if (!occupancy_units(k, p, di, bps, units)) return false;
     p.units = units < M ? units : M;
+    // the RMSNorm backward without clusters hands the last rows of its grid out
+    // from the row pool (pool.h), when the pool kernel (one producer warp more per
+    // CTA) keeps the same residency
+    if (pass == 1 && cl == 1 && g_row_pool && stages >= 2 && stages <= kPoolMaxStages &&
+        threads <= kTmaMaxThreads && vpt <= 4) {
+        Plan q = p;
+        q.extra_threads = 32;
+        q.pool = make_row_pool(M, p.units, g_pool_shape);
+        const void* kq = q.pool.head > 0 ? kernel_for(pass, q) : nullptr;
+        int64_t uq = 0;
+        if (kq && prepare_kernel(kq, dev, di) && occupancy_units(kq, q, di, bps, uq) && uq >= p.units) p = q;
+        (void)cudaGetLastError();
+    }
     return true;
 }
 
@@ -715,9 +748,16 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     const int layout = a16 ? kLayoutAligned : (same_phase ? kLayoutPhase : kLayoutMixed);
     CallPlan c;
     if ((st = plan_call(1, M, static_cast<int>(N), dtype, offset, layout, c)) != RMSNORM_OK) return st;
+    // a workspace too small for the row pool's partial rows but large enough for
+    // one row per CTA takes the static assignment (same kernels otherwise)
+    if (c.plan.pool.head > 0 && workspace_bytes < workspace_need(c.plan, N)) {
+        Plan q = c.plan;
+        q.pool = RowPool{};
+        q.extra_threads = 0;
+        if (workspace_bytes >= workspace_need(q, N)) c.plan = q;
+    }
     const Plan& p = c.plan;
-    const size_t need = static_cast<size_t>(p.units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
-    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_need(p, N)) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
     a.x = x;
     a.gamma = gamma;
@@ -733,8 +773,14 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
     a.lddx = lddx;
     a.stages = p.stages;
     a.err = c.err;
+    a.pool = p.pool;
+    if (p.pool.head > 0) {
+        a.queue = reinterpret_cast<unsigned long long*>(a.ws + partial_rows(p) * a.ldws);
+        a.ticket = next_call_ticket();
+    }
     if (launch_pass(1, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, dgamma, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, partial_rows(p), a.N, a.ldws, dgamma, cs) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -916,13 +962,13 @@ extern "C" size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype
     int dev = 0;
     DeviceInfo* di = nullptr;
     if (current_device(dev, di) != RMSNORM_OK) return 0;
-    int64_t units = 0;
+    size_t need = 0;
     Plan p;
     for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
         for (int off = 0; off < 2; ++off)
-            if (get_plan(1, M, static_cast<int>(N), dtype, off, layout, dev, *di, p) && p.units > units)
-                units = p.units;
-    return static_cast<size_t>(units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
+            if (get_plan(1, M, static_cast<int>(N), dtype, off, layout, dev, *di, p))
+                need = std::max(need, workspace_need(p, N));
+    return need;
 }
 
 extern "C" rmsnorm_status rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd,
@@ -1033,6 +1079,10 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
     const int layout = aligned16 == 1 ? kLayoutAligned : (aligned16 == 0 ? kLayoutPhase : kLayoutMixed);
     if (!get_plan(pass, M > 0 ? M : 1, static_cast<int>(N), dtype, 0, layout, dev, *di, p))
         return RMSNORM_ERR_UNSUPPORTED;
+    char pool_text[64] = "";
+    if (p.pool.head > 0)
+        snprintf(pool_text, sizeof pool_text, " pool_head=%lld pool_segments=%lld", static_cast<long long>(p.pool.head),
+                 static_cast<long long>(p.pool.nseg));
     if (p.path == kPathRowVec)
         snprintf(buf, buf_len, "rowvec threads=%d kv=%d units=%lld smem=%zu sms=%d", p.threads, p.per_thread,
                  static_cast<long long>(p.units), p.smem, di->sms);
@@ -1043,11 +1093,52 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
         snprintf(buf, buf_len, "ragged threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.threads,
                  p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
     else if (p.path == kPathTma)
-        snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d", p.cluster,
-                 p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms);
+        snprintf(buf, buf_len, "tma cluster=%d threads=%d vpt=%d stages=%d units=%lld smem=%zu sms=%d%s", p.cluster,
+                 p.threads, p.per_thread, p.stages, static_cast<long long>(p.units), p.smem, di->sms, pool_text);
     else
         snprintf(buf, buf_len, "scalar threads=%d units=%lld smem=%zu sms=%d", p.threads,
                  static_cast<long long>(p.units), p.smem, di->sms);
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_set_row_pool(int enabled) {
+    if (enabled != 0 && enabled != 1) return RMSNORM_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_row_pool = enabled != 0;
+    ++g_override_gen;
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_set_row_pool_shape(int head_pct, int head_pct_few, int len_max, int len_min) {
+    if (head_pct < 0 || head_pct > 99 || head_pct_few < 0 || head_pct_few > 99 || len_max < 0 || len_min < 0 ||
+        len_max > 1024 || len_min > 1024)
+        return RMSNORM_ERR_ARG;
+    const RowPoolShape d;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_pool_shape.head_pct = head_pct ? head_pct : d.head_pct;
+    g_pool_shape.head_pct_few = head_pct_few ? head_pct_few : d.head_pct_few;
+    g_pool_shape.len_max = len_max ? len_max : d.len_max;
+    g_pool_shape.len_min = len_min ? len_min : d.len_min;
+    if (g_pool_shape.len_min > g_pool_shape.len_max) g_pool_shape.len_min = g_pool_shape.len_max;
+    ++g_override_gen;
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_row_pool_layout(int64_t M, int64_t G, int64_t* head, int64_t* nseg) {
+    if (!head || !nseg) return RMSNORM_ERR_NULL;
+    if (M < 0 || G < 1) return RMSNORM_ERR_ARG;
+    const RowPool p = make_row_pool(M, G);
+    *head = p.head;
+    *nseg = p.nseg;
+    return RMSNORM_OK;
+}
+
+extern "C" rmsnorm_status rmsnorm_row_pool_segment(int64_t M, int64_t G, int64_t k, int64_t* first, int64_t* last) {
+    if (!first || !last) return RMSNORM_ERR_NULL;
+    if (M < 0 || G < 1) return RMSNORM_ERR_ARG;
+    const RowPool p = make_row_pool(M, G);
+    if (k < 0 || k >= p.nseg) return RMSNORM_ERR_ARG;
+    pool_segment(p, k, *first, *last);
     return RMSNORM_OK;
 }
 

@@ -235,6 +235,320 @@ __global__ void __launch_bounds__(BwdTmaBounds<DT, VPT, CLUSTER>::threads, (BwdT
     }
 }
 
+// The pool's queue word holds {ticket (high 32 bits), segments taken (low 32)}.
+// It is this call's when it carries the call's ticket and a count of at most
+// nseg + 2G (a CTA stops after its first take past the end, and makes at most one
+// extra take while the word is being opened); anything else -- a word left by an
+// earlier call, never written, or holding another tensor's bytes -- is not.
+__device__ __forceinline__ bool pool_word_ours(unsigned long long w, uint32_t ticket, int64_t nseg, int64_t G) {
+    return (w >> 32) == ticket && static_cast<int64_t>(w & 0xffffffffull) <= nseg + 2 * G;
+}
+
+// CTA 0, at the start: make the word this call's with no segment taken (one
+// compare-and-swap from whatever it holds to {ticket, 0}; bounded retries).
+__device__ __forceinline__ void pool_open(unsigned long long* q, uint32_t ticket, int64_t nseg, int64_t G,
+                                          uint32_t* err) {
+    const unsigned long long mine = static_cast<unsigned long long>(ticket) << 32;
+    unsigned long long w = __ldcg(q);
+#pragma unroll 1
+    for (uint32_t i = 0; i < kWaitPollLimit; ++i) {
+        if (pool_word_ours(w, ticket, nseg, G)) return;
+        const unsigned long long prev = atomicCAS(q, w, mine);
+        if (prev == w) return;
+        w = prev;
+    }
+    atomicOr(err, kDevErrWaitTimeout);
+}
+
+// The segment a take got, from the value `old` its fetch-and-add returned; -1
+// when the queue is empty. Takes are single fetch-and-adds, issued ahead of need
+// so that their round trip overlaps rows still in the ring (a compare-and-swap
+// loop here serialises the CTAs that take at once). An add that found the word
+// not yet this call's (CTA 0 had not opened it) opens it itself, taking segment
+// 0, or adds again once another CTA has; bounded, and on exhaustion the timeout
+// bit is set and the CTA takes no more segments (the others still empty the queue).
+__device__ __forceinline__ int64_t pool_segment_of(unsigned long long old, unsigned long long* q, uint32_t ticket,
+                                                   int64_t nseg, int64_t G, uint32_t* err) {
+    if (pool_word_ours(old, ticket, nseg, G)) {
+        const int64_t k = static_cast<int64_t>(old & 0xffffffffull);
+        return k < nseg ? k : -1;
+    }
+    const unsigned long long mine = static_cast<unsigned long long>(ticket) << 32;
+    unsigned long long w = old + 1;  // the word after this CTA's add, unless others added too
+#pragma unroll 1
+    for (uint32_t i = 0; i < kWaitPollLimit; ++i) {
+        const unsigned long long prev = atomicCAS(q, w, mine | 1ull);
+        if (prev == w) return 0;
+        if (pool_word_ours(prev, ticket, nseg, G)) {
+            const int64_t k = static_cast<int64_t>(atomicAdd(q, 1ull) & 0xffffffffull);
+            return k < nseg ? k : -1;
+        }
+        w = prev;
+    }
+    atomicOr(err, kDevErrWaitTimeout);
+    return -1;
+}
+
+// Bounded wait on an mbarrier phase that also gives up as soon as `abort` is
+// set (by a thread whose own wait gave up); sets the timeout bit on exhaustion.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint32_t* err,
+                                                   volatile int* abort) {
+#pragma unroll 1
+    for (uint32_t i = 0; i < kWaitPollLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    atomicOr(err, kDevErrWaitTimeout);
+    return false;
+}
+
+// Backward row kernel with the row pool of pool.h (no clusters), formulas as in
+// bwd_tma_kernel. CTA b first takes rows b + j * G, j < a.pool.head (dgamma
+// partial row b), then segments of consecutive rows from the queue (partial row
+// G + k for segment k); CTA 0 opens the queue for this call as it starts.
+//
+// The CTA is a.threads consumer threads plus one producer warp. The producer's
+// lane 0 runs the ring ahead of the consumers: for each stage it waits until every
+// consumer warp has released the stage's previous row (the `empty` barrier, one
+// arrival per consumer warp), decides the next row (head, then queue; the take is
+// issued kPoolTakeAhead rows before it is needed), records the row and the partial
+// row to write after it in shared memory, and issues the TMA copies of x and dy
+// and a 4-byte cp.async of the row's r, all completing on the stage's `full`
+// barrier (two arrivals: the copies' expect_tx and the cp.async). A stage with no
+// row (queue empty) is completed by plain arrivals and ends both loops. The
+// consumers' only barrier per row is a named barrier among themselves (the row
+// sum), so the producer's bookkeeping never delays a row.
+// At most 128 registers (no spills at up to four vectors per thread): three CTAs of
+// 128 consumer threads and the producer warp then fit an SM.
+template <int DT, int VPT, bool OFFSET>
+__global__ void __maxnreg__(128) bwd_pool_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int64_t stage_row[kPoolMaxStages];
+    __shared__ int64_t stage_unit[kPoolMaxStages];
+    __shared__ float stage_r[kPoolMaxStages];
+    __shared__ uint64_t empty[kPoolMaxStages];
+
+    const int tid = threadIdx.x;
+    const int nc = blockDim.x - 32;  // consumer threads
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int ncw = nc >> 5;         // consumer warps; the producer is warp ncw
+    const int64_t G = gridDim.x;
+
+    const int nvec = a.N / VEC;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * E::kBytes;
+    const uint32_t stage_bytes = 2 * row_bytes;  // x row, then dy row
+    const int S = a.stages;
+
+    // shared memory: ring | gamma in fp32 | full barriers | warp partials [2][32] | abort flag
+    unsigned char* ring = smem;
+    float* gsm = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(gsm + a.N);
+    float* red = reinterpret_cast<float*>(full + S);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 2);
+            mbar_init(smem_u32(&empty[s]), static_cast<uint32_t>(ncw));
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+
+    if (warp == ncw) {
+        // ---------------- producer ----------------
+        if (lane != 0) return;
+        const uint32_t ticket = static_cast<uint32_t>(a.ticket);
+        const uint64_t pol = l2_evict_first_policy();
+        const char* xb = static_cast<const char*>(a.x);
+        const char* dyb = static_cast<const char*>(a.dy);
+        const size_t x_pitch = static_cast<size_t>(a.ldx) * E::kBytes;
+        const size_t dy_pitch = static_cast<size_t>(a.lddy) * E::kBytes;
+        int64_t heads = 0, seg_row = 0, seg_end = 0, seg_id = -1;
+        unsigned long long pend = 0;
+        bool pend_on = false;
+        auto take_ahead = [&]() {
+            if (!pend_on) {
+                pend = atomicAdd(a.queue, 1ull);
+                pend_on = true;
+            }
+        };
+        int64_t issued = 0;
+        bool aborted = false;
+        for (;; ++issued) {
+            const int s = static_cast<int>(issued % S);
+            const int64_t round = issued / S;
+            if (round > 0 &&
+                !mbar_wait_or_abort(smem_u32(&empty[s]), static_cast<uint32_t>((round - 1) & 1), a.err,
+                                    abort_flag)) {
+                aborted = true;
+                break;
+            }
+            int64_t row = -1, unit = -1;
+            if (heads < a.pool.head) {
+                row = static_cast<int64_t>(blockIdx.x) + heads * G;
+                if (++heads == a.pool.head) unit = blockIdx.x;
+                if (a.pool.head - heads <= kPoolTakeAhead) take_ahead();
+            } else if (seg_id != -2) {
+                if (seg_row >= seg_end) {
+                    take_ahead();
+                    pend_on = false;
+                    const int64_t k = pool_segment_of(pend, a.queue, ticket, a.pool.nseg, G, a.err);
+                    if (k >= 0) pool_segment(a.pool, k, seg_row, seg_end);
+                    seg_id = k >= 0 ? k : -2;
+                }
+                if (seg_id >= 0) {
+                    row = seg_row++;
+                    if (seg_row == seg_end) unit = G + seg_id;
+                    if (seg_end - seg_row <= kPoolTakeAhead) take_ahead();
+                }
+            }
+            stage_row[s] = row;
+            stage_unit[s] = unit;
+            const uint32_t bar = smem_u32(&full[s]);
+            if (row < 0) {
+                mbar_arrive_n(bar, 2);
+                break;
+            }
+            unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+            cp_async4(smem_u32(&stage_r[s]), a.rstd_in + row);
+            cp_async_arrive_noinc(bar);
+            mbar_arrive_expect_tx(bar, stage_bytes);
+            bulk_g2s_in(smem_u32(st), xb + static_cast<size_t>(row) * x_pitch, row_bytes, bar, pol, a.x, a.M,
+                        a.ldx, a.N, E::kBytes, a.err);
+            bulk_g2s_in(smem_u32(st + row_bytes), dyb + static_cast<size_t>(row) * dy_pitch, row_bytes, bar, pol,
+                        a.dy, a.M, a.lddy, a.N, E::kBytes, a.err);
+            if (issued == 0 && blockIdx.x == 0) pool_open(a.queue, ticket, a.pool.nseg, G, a.err);
+        }
+        if (aborted) {
+            // the consumers gave up: wait for the copies of the stages issued last
+            // (at most S of them may still be in flight) before the CTA exits
+            for (int64_t i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
+                if (stage_row[i % S] >= 0)
+                    mbar_wait_bounded(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), a.err,
+                                      1u << 16);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    // gamma widened once (offset variant: 1 + w), VEC/4 planes of float4
+    float4* gsm4 = reinterpret_cast<float4*>(gsm);
+    {
+        const uint4* gs = reinterpret_cast<const uint4*>(a.gamma);
+        for (int idx = tid; idx < nvec; idx += nc) {
+            float w[VEC];
+            E::unpack(__ldg(gs + idx), w);
+#pragma unroll
+            for (int q = 0; q < VEC; q += 4) {
+                float4 f = OFFSET ? make_float4(1.0f + w[q], 1.0f + w[q + 1], 1.0f + w[q + 2], 1.0f + w[q + 3])
+                                  : make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+                gsm4[(q / 4) * nvec + idx] = f;
+            }
+        }
+    }
+    float acc[VPT][VEC];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
+    named_barrier_sync(1, nc);  // gamma planes are visible to every consumer
+
+    char* dxb = static_cast<char*>(a.dx);
+    const size_t dx_pitch = static_cast<size_t>(a.lddx) * E::kBytes;
+    // partial rows are read back by the column reduce right after this kernel:
+    // keep them in L2 while the ring streams x and dy through it (bf16 65536x4096
+    // backward 246.6 -> 242.8 us, fp16 16384x8192 133.4 -> 133.2)
+    const uint64_t keep = l2_evict_last_policy();
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t j = 0;; ++j) {
+        if (!mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
+        const int64_t row = stage_row[s];
+        const int64_t unit = stage_unit[s];
+        if (row < 0) break;  // the queue is empty (every consumer reads the same stage)
+        const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+        const float r = stage_r[s];
+
+        float xf[VPT][VEC], uf[VPT][VEC];
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nc + tid;
+            float df[VEC], g[VEC];
+            if (idx < nvec) {
+                E::unpack(*reinterpret_cast<const uint4*>(st + idx * 16), xf[v]);
+                E::unpack(*reinterpret_cast<const uint4*>(st + row_bytes + idx * 16), df);
+#pragma unroll
+                for (int q = 0; q < VEC; q += 4) {
+                    const float4 f = gsm4[(q / 4) * nvec + idx];
+                    g[q] = f.x; g[q + 1] = f.y; g[q + 2] = f.z; g[q + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) xf[v][e] = df[e] = g[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                uf[v][e] = __fmul_rn(df[e], g[e]);
+                if (e & 1) p1 = fmaf(uf[v][e], xf[v][e], p1); else p0 = fmaf(uf[v][e], xf[v][e], p0);
+                acc[v][e] = fmaf(__fmul_rn(df[e], xf[v][e]), r, acc[v][e]);
+            }
+        }
+        // this warp is done with the stage: the producer may refill it once every
+        // consumer warp has said so
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        float* redb = red + (j & 1) * 32;
+        const float wsum = warp_allsum(p0 + p1);
+        if (lane == 0) redb[warp] = wsum;
+        named_barrier_sync(1, nc);
+        if (*abort_flag) break;  // every consumer reads the flag after the same barrier
+
+        float t = lane < ncw ? redb[lane] : 0.f;
+        t = warp_allsum(t);
+        const float c = t / static_cast<float>(a.N);
+        // dx = r*u - x*k with k = r^3 * c, as one fused multiply-add per element
+        const float k = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), c);
+        char* dxrow = dxb + static_cast<size_t>(row) * dx_pitch;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nc + tid;
+            if (idx < nvec) {
+                float o[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) o[e] = fmaf(-xf[v][e], k, __fmul_rn(r, uf[v][e]));
+                stg128(dxrow + idx * 16, E::pack(o));
+            }
+        }
+        // the last row of a head or a segment: its partial row, then fresh sums
+        if (unit >= 0) {
+            float* wrow = a.ws + static_cast<size_t>(unit) * a.ldws;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int idx = v * nc + tid;
+                if (idx < nvec) {
+#pragma unroll
+                    for (int q = 0; q < VEC; q += 4)
+                        stg_f4_hint(wrow + idx * VEC + q, acc[v][q], acc[v][q + 1], acc[v][q + 2], acc[v][q + 3], keep);
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[v][e] = 0.f;
+            }
+        }
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+    griddep_launch_dependents();
+}
+
 // General path: any N, any element alignment. One CTA per row (persistent);
 // thread t owns columns t, t + nt, ...; two passes over the row (the second is
 // served by L1/L2); dgamma accumulators live in shared memory indexed by column
@@ -305,8 +619,9 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 
 // dgamma[j] = sum_{p < units} ws[p][j] in a fixed order, without atomics.
 // A block owns an 8-column tile (two float4 lanes) of the partial rows and
-// 128 row lanes: lane (cq, rq) of warp w owns columns 4cq..4cq+3 and rows
-// ry = 16w + rq, ry + 128, ... Partial rows are ldws floats apart, ldws a
+// 16 * WARPS row lanes: lane (cq, rq) of warp w owns columns 4cq..4cq+3 and rows
+// ry = 16w + rq, ry + 16 * WARPS, ... (8 warps; 16 when there are more than 1024
+// partial rows, so that one batch of loads still covers them). Partial rows are ldws floats apart, ldws a
 // multiple of 4, so every load is a 16-byte float4 (the up to three pad columns
 // after N are read but never stored). Each thread issues kReduceBatch loads
 // before adding any of them, so a launch keeps the whole workspace in flight:
@@ -314,19 +629,19 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 // latency, not bandwidth (ncu at 456 partial rows of 4096: 3.8 us, against
 // 4.5 us for 32-column tiles split over 4-CTA clusters; an empty kernel takes
 // 1.8 us). The row sums are combined in a fixed tree: in row order within a
-// thread, a butterfly over the 16 row lanes of a warp, then the 8 warps in
+// thread, a butterfly over the 16 row lanes of a warp, then the warps in
 // order through shared memory; the result is rounded once into the I/O dtype.
 // The order depends only on (units, N), so dgamma is bitwise reproducible.
 // units == 0 (no rows) writes zeros. blockIdx.y = 1 sums the second plane
 // (LayerNorm's dbeta partials) into out1.
 constexpr int kReduceBatch = 8;
-constexpr int kReduceLanes = 2;                  // float4 lanes per row: 8 columns
-constexpr int kReduceRows = 256 / kReduceLanes;  // row lanes per block
-template <int DT>
-__global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int64_t units, int N, int64_t ldws,
-                                                           void* out0, void* out1) {
+constexpr int kReduceLanes = 2;  // float4 lanes per row: 8 columns
+template <int DT, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
+                                                                  int64_t ldws, void* out0, void* out1) {
     using E = Elem<DT>;
-    __shared__ float4 part[8][kReduceLanes];
+    constexpr int kReduceRows = 32 * WARPS / kReduceLanes;  // row lanes per block
+    __shared__ float4 part[WARPS][kReduceLanes];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int cq = lane % kReduceLanes;
@@ -366,7 +681,7 @@ __global__ void __launch_bounds__(256) dgamma_reduce_kernel(const float* ws, int
     if (threadIdx.x < kReduceLanes) {
         float4 t = part[0][threadIdx.x];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) {
+        for (int w = 1; w < WARPS; ++w) {
             const float4 u = part[w][threadIdx.x];
             t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
@@ -392,7 +707,17 @@ static const void* bwd_tma_vpt(int vpt) {
     }
 }
 template <int DT, bool OFF>
-static const void* bwd_tma_for(int vpt, int cluster) {
+static const void* bwd_pool_vpt(int vpt) {
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&bwd_pool_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&bwd_pool_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&bwd_pool_kernel<DT, 4, OFF>);
+    default: return nullptr;
+    }
+}
+template <int DT, bool OFF>
+static const void* bwd_tma_for(int vpt, int cluster, bool pool) {
+    if (pool) return bwd_pool_vpt<DT, OFF>(vpt);
     return cluster > 1 ? bwd_tma_vpt<DT, OFF, true>(vpt) : bwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
@@ -402,10 +727,11 @@ static const void* bwd_scalar_for() {
 template <bool OFF>
 static const void* bwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
+    const bool pool = p.pool.head > 0 && p.cluster == 1;
     switch (p.dtype) {
-    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF32, OFF>();
-    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kF16, OFF>();
-    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : bwd_scalar_for<kBF16, OFF>();
+    case kF32: return tma ? bwd_tma_for<kF32, OFF>(p.per_thread, p.cluster, pool) : bwd_scalar_for<kF32, OFF>();
+    case kF16: return tma ? bwd_tma_for<kF16, OFF>(p.per_thread, p.cluster, pool) : bwd_scalar_for<kF16, OFF>();
+    case kBF16: return tma ? bwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster, pool) : bwd_scalar_for<kBF16, OFF>();
     default: return nullptr;
     }
 }
@@ -417,19 +743,29 @@ const void* bwd_kernel(const Plan& p) {
     return p.offset ? bwd_pick<true>(p) : bwd_pick<false>(p);
 }
 
-const void* dgamma_reduce_kernel_ptr(int dtype) {
+template <int WARPS>
+static const void* dgamma_reduce_for(int dtype) {
     switch (dtype) {
-    case kF32: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF32>);
-    case kF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF16>);
-    case kBF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kBF16>);
+    case kF32: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF32, WARPS>);
+    case kF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kF16, WARPS>);
+    case kBF16: return reinterpret_cast<const void*>(&dgamma_reduce_kernel<kBF16, WARPS>);
     default: return nullptr;
     }
 }
 
+// Warps per block of the column reduce: 16 (256 row lanes) above 1024 partial
+// rows, so that one batch of kReduceBatch loads per lane still covers them.
+int dgamma_reduce_warps(int64_t units) { return units > 1024 ? 16 : 8; }
+
+const void* dgamma_reduce_kernel_ptr(int dtype, int64_t units) {
+    return dgamma_reduce_warps(units) == 16 ? dgamma_reduce_for<16>(dtype) : dgamma_reduce_for<8>(dtype);
+}
+
+
 cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.units * p.cluster), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads + p.extra_threads), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -452,11 +788,11 @@ cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStre
 
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
                                  cudaStream_t s, void* dbeta) {
-    const void* k = dgamma_reduce_kernel_ptr(dtype);
+    const void* k = dgamma_reduce_kernel_ptr(dtype, units);
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((N + 4 * kReduceLanes - 1) / (4 * kReduceLanes)), dbeta ? 2u : 1u, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * dgamma_reduce_warps(units)), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

@@ -191,6 +191,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Barrier `id` (1-15; 0 is __syncthreads) among `count` threads of the CTA, a
+// multiple of 32; the other threads are not involved.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive without a transaction count (completes a phase whose count is 1).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -219,6 +230,21 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+// L2 policy for data read back soon by another kernel (the dgamma partial rows
+// the column reduce reads right after the row kernel).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte global store of four floats with an L2 cache policy.
+__device__ __forceinline__ void stg_f4_hint(float* p, float a, float b, float c, float d, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "l"(policy)
+                 : "memory");
 }
 
 // TMA bulk copy global -> shared, completion counted in bytes on `bar`.
@@ -312,6 +338,21 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Asynchronous 4-byte copy global -> shared (cp.async, cached at L1), and an
+// arrive on `bar` once every cp.async this thread issued so far has landed; the
+// arrive does not add to the barrier's expected count (it is one of the counts
+// given at init).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Arrive `count` times at once, without a transaction count.
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
 // 16-byte global stores: default caching, and cache-streaming (evict-first).

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pool.h"
+
 namespace rmsnorm {
 
 // Arguments of every row kernel (forward and backward use disjoint subsets).
@@ -33,6 +35,11 @@ struct RowArgs {
     float eps;
     int stages;            // TMA pipeline depth
     uint32_t* err;         // device error word
+    RowPool pool;          // backward row pool (pool.head == 0: static assignment)
+    unsigned long long* queue;  // the pool's queue word, after the partial rows:
+                                // {call ticket (high 32 bits), segments taken}
+    unsigned long long ticket;  // this call's ticket (low 32 bits used; consecutive
+                                // calls in a process never share one)
 };
 
 enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2, kPathRagged = 3, kPathLanes = 4 };
@@ -64,6 +71,11 @@ constexpr int kLaneMaxRowBytes = 2048;
 // three.
 constexpr int kRaggedDbwdMaxThreads = 320;
 constexpr int kScalarThreads = 256;
+// Ring stages the pool kernel keeps row records for (bwd.cu, bwd_pool_kernel), and
+// how many rows before the end of its head or segment a CTA takes its next segment
+// (the take's round trip then overlaps those rows).
+constexpr int kPoolMaxStages = 8;
+constexpr int kPoolTakeAhead = 2;
 
 // A launch shape chosen by the planner.
 struct Plan {
@@ -77,7 +89,14 @@ struct Plan {
     size_t smem = 0;       // dynamic shared memory per CTA
     int64_t units = 0;     // clusters (TMA) or CTAs (scalar) = rows of dgamma partials
     int lanes = 0;         // narrow-row path: lanes per row (per_thread: vectors per lane)
+    RowPool pool;          // RMSNorm backward, TMA path without clusters: the row pool
+    int extra_threads = 0; // threads per CTA beyond `threads` (the pool kernel's producer warp)
 };
+
+// Rows of dgamma partials a plan writes, and the workspace bytes it needs: one
+// partial row per CTA (cluster) and per pool segment, each ldws floats, then the
+// pool's 16-byte queue word.
+inline int64_t partial_rows(const Plan& p) { return p.units + p.pool.nseg; }
 
 // Kernel entry for a plan (used for occupancy queries and attributes).
 const void* fwd_kernel(const Plan& p);
@@ -91,7 +110,7 @@ const void* ln_rowvec_kernel(int pass, const Plan& p);  // pass 2 forward, 3 bac
 const void* lanes_kernel(int pass, const Plan& p);    // narrow rows, passes 0-4
 const void* dbwd_kernel(const Plan& p);               // RMSNorm double backward (TMA, ragged or scalar path)
 const void* dbwd_ragged_kernel_ptr(const Plan& p);    // its ragged TMA kernel
-const void* dgamma_reduce_kernel_ptr(int dtype);
+const void* dgamma_reduce_kernel_ptr(int dtype, int64_t units);  // launch shape depends on the row count
 
 // Launch `k` with the plan's grid, block, shared memory and cluster shape, and
 // programmatic stream serialization.
@@ -101,6 +120,11 @@ cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStre
 // other; ldws a multiple of 4).
 // Floats between the workspace's partial rows for rows of N elements.
 inline int64_t workspace_pitch(int64_t N) { return (N + 3) / 4 * 4; }
+inline size_t workspace_need(const Plan& p, int64_t N, int planes = 1) {
+    return static_cast<size_t>(planes) * static_cast<size_t>(partial_rows(p)) *
+               static_cast<size_t>(workspace_pitch(N)) * sizeof(float) +
+           (p.pool.nseg > 0 ? 16 : 0);
+}
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
                                  cudaStream_t s, void* dbeta = nullptr);
 

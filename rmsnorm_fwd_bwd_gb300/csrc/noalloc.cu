@@ -42,11 +42,12 @@ extern "C" rmsnorm_status rmsnorm_bwd_static_scratch(const void* dy, const void*
     void* scratch = nullptr;
     const rmsnorm_status st = scratch_address(&scratch);
     if (st != RMSNORM_OK) return st;
-    // rmsnorm_bwd rejects (RMSNORM_ERR_WORKSPACE) any shape whose partial sums
-    // need more than RMSNORM_STATIC_SCRATCH_BYTES, before launching anything.
+    // rmsnorm_bwd runs without the row queue when the queue's partial rows do not
+    // fit RMSNORM_STATIC_SCRATCH_BYTES, and rejects (RMSNORM_ERR_WORKSPACE) any
+    // shape whose partial sums need more even then, before launching anything.
     // Every partial-sum row the column reduction reads is first written by the
-    // row kernel of the same call, so nothing left over from an earlier call is
-    // read and nothing needs clearing.
+    // row kernel of the same call, and a queue word left by an earlier call holds
+    // that call's ticket, which starts a fresh queue: nothing needs clearing.
     return rmsnorm_bwd(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, offset, scratch,
                        RMSNORM_STATIC_SCRATCH_BYTES, stream);
 }

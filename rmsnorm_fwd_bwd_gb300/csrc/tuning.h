@@ -25,6 +25,28 @@ extern "C" {
 rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int stages,
                                            int blocks_per_sm);
 
+/*
+ * Turn the RMSNorm backward's row pool on (1, the default) or off (0: every CTA
+ * takes the rows b, b + G, ... of the static assignment). Process-wide, like the
+ * override above; for comparing the two assignments.
+ */
+rmsnorm_status rmsnorm_set_row_pool(int enabled);
+
+/*
+ * Shape of the row pool for later plans: percent of the rows in the per-CTA heads
+ * (at >= 64 and at < 64 rows per CTA) and the longest and shortest segment
+ * length; 0 keeps a default (85, 90, 16, 4). Process-wide, for tuning.
+ */
+rmsnorm_status rmsnorm_set_row_pool_shape(int head_pct, int head_pct_few, int len_max, int len_min);
+
+/*
+ * The row pool of M rows over G CTAs (head rows per CTA, segments in the queue;
+ * head = 0: no pool), and rows [*first, *last) of its segment k. Host-only
+ * arithmetic, no GPU needed.
+ */
+rmsnorm_status rmsnorm_row_pool_layout(int64_t M, int64_t G, int64_t* head, int64_t* nseg);
+rmsnorm_status rmsnorm_row_pool_segment(int64_t M, int64_t G, int64_t k, int64_t* first, int64_t* last);
+
 #ifdef __cplusplus
 }
 #endif

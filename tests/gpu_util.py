@@ -48,12 +48,16 @@ def _place(arr, dtype, misalign):
     return buf, buf[1:]
 
 
-def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, stream=None):
+def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, stream=None, ws_fill=None,
+        ws_bytes=None):
     """Forward (and backward) through the C ABI. Returns numpy storage arrays
     (y, rstd, dx, dgamma); dx/dgamma are None when do_bwd is False.
 
     misalign: False, True (every tensor one element off a 16-byte boundary) or a
-    set of names among {"x", "g", "dy", "y", "dx"} to shift only those."""
+    set of names among {"x", "g", "dy", "y", "dx"} to shift only those.
+    ws_fill: None (the workspace as torch.empty leaves it), a byte value, or
+    "random" (seeded random bytes); ws_bytes: the workspace size passed to the
+    backward (default: rmsnorm_bwd_workspace_size)."""
     torch = _torch()
     M, N = x.shape
     names = {"x", "g", "dy", "y", "dx"} if misalign is True else set(misalign or ())
@@ -78,8 +82,13 @@ def run(x, g, dy, dtype, offset=False, eps=1e-6, misalign=False, do_bwd=True, st
             b2 = torch.empty(M * N + 2 * GUARD + 1, dtype=dxt.dtype, device=dxt.device)
             b2[1:] = dxbuf
             dxbuf, dxt = b2[1:], b2[1 + GUARD:1 + GUARD + M * N]
-        wsz = B.rmsnorm_bwd_workspace_size(M, N, dtype)
+        wsz = B.rmsnorm_bwd_workspace_size(M, N, dtype) if ws_bytes is None else int(ws_bytes)
         ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device="cuda")
+        if ws_fill == "random":
+            gen = torch.Generator(device="cuda").manual_seed(1234)
+            ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda", generator=gen))
+        elif ws_fill is not None:
+            ws.fill_(int(ws_fill))
         st = B.rmsnorm_bwd(dyt, xt, gt, rstd, dxt, dgt, M, N, dtype, int(offset), ws, wsz, stream)
         assert st == B.RMSNORM_OK, B.rmsnorm_status_string(st)
     torch.cuda.synchronize()
