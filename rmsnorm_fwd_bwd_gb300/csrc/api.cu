@@ -779,7 +779,8 @@ rmsnorm_status bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t ldx
         a.ticket = next_call_ticket();
     }
     if (launch_pass(1, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, partial_rows(p), a.N, a.ldws, dgamma, cs) != cudaSuccess)
+    if (launch_dgamma_reduce(dtype, a.ws, partial_rows(p), a.N, a.ldws, dgamma, cs, nullptr, a.queue) !=
+        cudaSuccess)
         return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }

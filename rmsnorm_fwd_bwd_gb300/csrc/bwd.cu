@@ -636,9 +636,12 @@ __global__ void __launch_bounds__(kScalarThreads) bwd_scalar_kernel(const RowArg
 // (LayerNorm's dbeta partials) into out1.
 constexpr int kReduceBatch = 8;
 constexpr int kReduceLanes = 2;  // float4 lanes per row: 8 columns
+// `queue` (may be null): the row pool's queue word, closed here once the row
+// kernel has finished (see kPoolClosed in pool.h).
 template <int DT, int WARPS>
 __global__ void __launch_bounds__(32 * WARPS) dgamma_reduce_kernel(const float* ws, int64_t units, int N,
-                                                                  int64_t ldws, void* out0, void* out1) {
+                                                                  int64_t ldws, void* out0, void* out1,
+                                                                  unsigned long long* queue) {
     using E = Elem<DT>;
     constexpr int kReduceRows = 32 * WARPS / kReduceLanes;  // row lanes per block
     __shared__ float4 part[WARPS][kReduceLanes];
@@ -650,6 +653,7 @@ __global__ void __launch_bounds__(32 * WARPS) dgamma_reduce_kernel(const float* 
     void* dgamma = blockIdx.y == 0 ? out0 : out1;
     if (blockIdx.y != 0) ws += units * ldws;
     griddep_wait();  // the partial sums come from the row kernel just before
+    if (queue && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *queue = kPoolClosed;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < N) {
         for (int64_t base = ry; base < units; base += kReduceRows * kReduceBatch) {
@@ -787,7 +791,7 @@ cudaError_t launch_rows(const void* k, const Plan& p, const RowArgs& a, cudaStre
 }
 
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
-                                 cudaStream_t s, void* dbeta) {
+                                 cudaStream_t s, void* dbeta, unsigned long long* queue) {
     const void* k = dgamma_reduce_kernel_ptr(dtype, units);
     if (!k) return cudaErrorInvalidDeviceFunction;
     cudaLaunchConfig_t cfg = {};
@@ -800,7 +804,7 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* params[] = {const_cast<float**>(&ws), &units, &N, &ldws, &dgamma, &dbeta};
+    void* params[] = {const_cast<float**>(&ws), &units, &N, &ldws, &dgamma, &dbeta, &queue};
     return cudaLaunchKernelExC(&cfg, k, params);
 }
 

@@ -125,8 +125,9 @@ inline size_t workspace_need(const Plan& p, int64_t N, int planes = 1) {
                static_cast<size_t>(workspace_pitch(N)) * sizeof(float) +
            (p.pool.nseg > 0 ? 16 : 0);
 }
+// `queue`: the row pool's queue word to close once the row kernel is done (or null).
 cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int N, int64_t ldws, void* dgamma,
-                                 cudaStream_t s, void* dbeta = nullptr);
+                                 cudaStream_t s, void* dbeta = nullptr, unsigned long long* queue = nullptr);
 
 // Device address of the error word in the current context (nullptr on failure),
 // looked up on every call.

@@ -36,6 +36,11 @@ namespace rmsnorm {
 
 constexpr int kPoolTiers = 3;
 
+// The queue word after a call: the column reduce that follows the row kernel
+// stores this (a count no call can reach), so that the next call -- even a replay
+// of a captured CUDA graph, which repeats the same ticket -- opens a fresh queue.
+constexpr unsigned long long kPoolClosed = 0xffffffffull;
+
 struct RowPool {
     int64_t head = 0;                     // rows per CTA taken before the queue; 0: no pool
     int64_t nseg = 0;                     // segments in the queue

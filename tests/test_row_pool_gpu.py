@@ -140,3 +140,52 @@ def test_small_workspace_takes_the_static_assignment():
     # one byte less than that: rejected before any launch
     with pytest.raises(AssertionError, match="workspace"):
         gpu_util.run(x, g, dy, dtype, ws_bytes=small - 1)
+
+
+def test_pool_backward_replayed_from_a_cuda_graph():
+    """A captured forward + backward repeats the same call ticket on every replay;
+    the column reduce closes the queue word after each call, so every replay (with
+    new inputs copied into the captured buffers) gives the eager bits."""
+    torch = pytest.importorskip("torch")
+    from rmsnorm_fwd_bwd_gb300 import binding as B
+    M, N, dtype = BASE
+    assert "pool_head=" in _plan(M, N, dtype)
+    dev = [tuple(B.to_device(a.reshape(-1), dtype) for a in inputs.make_inputs(M, N, dtype, seed=40 + i))
+           for i in range(3)]
+    x, g, dy = (torch.empty_like(t) for t in dev[0])
+    y = torch.empty_like(x)
+    r = torch.empty(M, dtype=torch.float32, device="cuda")
+    dx = torch.empty_like(x)
+    dg = torch.empty_like(g)
+    wsz = B.rmsnorm_bwd_workspace_size(M, N, dtype)
+    ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+
+    def step():
+        assert B.rmsnorm_fwd(x, g, y, r, M, N, 1e-6, dtype, 0) == 0
+        assert B.rmsnorm_bwd(dy, x, g, r, dx, dg, M, N, dtype, 0, ws, wsz) == 0
+
+    def load(k):
+        for dst, src in zip((x, g, dy), dev[k]):
+            dst.copy_(src)
+
+    refs = []
+    for k in range(len(dev)):
+        load(k)
+        step()
+        torch.cuda.synchronize()
+        refs.append((dx.clone(), dg.clone()))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for k, (rdx, rdg) in enumerate(refs):
+            load(k)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(dx.view(torch.int16), rdx.view(torch.int16)), f"dx differs on replay {k}"
+            assert torch.equal(dg.view(torch.int16), rdg.view(torch.int16)), f"dgamma differs on replay {k}"
