@@ -893,7 +893,7 @@ def main(argv=None):
     ap.add_argument("--rows", type=int, default=None,
                     help="override the row count M (small cases for profiler captures)")
     ap.add_argument("--static-rows", action="store_true",
-                    help="RMSNorm backward without the row pool (every block keeps a fixed share of the rows)")
+                    help="RMSNorm forward and backward without the row pool (every block keeps a fixed share of the rows)")
     args = ap.parse_args(argv)
     import dataclasses
     from rmsnorm_fwd_bwd_gb300 import inputs

@@ -235,8 +235,9 @@ def rmsnorm_set_launch_override(pass_, threads=0, vpt=0, stages=0, blocks_per_sm
                                                int(blocks_per_sm))
 
 
-def rmsnorm_set_row_pool(enabled: bool) -> int:
-    return _load().rmsnorm_set_row_pool(int(bool(enabled)))
+def rmsnorm_set_row_pool(enabled) -> int:
+    """0/False: static rows; 1/True: the row pool; 2: pool with the forward's queue bypassed."""
+    return _load().rmsnorm_set_row_pool(int(enabled))
 
 
 def rmsnorm_set_row_pool_shape(head_pct=0, head_pct_few=0, len_max=0, len_min=0) -> int:

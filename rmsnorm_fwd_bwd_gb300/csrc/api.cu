@@ -86,7 +86,8 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 Override g_override[kPasses];
 unsigned g_override_gen = 0;
-bool g_row_pool = true;  // rmsnorm_set_row_pool
+int g_row_pool = 1;  // rmsnorm_set_row_pool: 0 off, 1 on, 2 on with the forward's queue bypassed
+std::atomic<unsigned> g_fwd_slot{0};  // the forward pool's next queue slot
 RowPoolShape g_pool_shape;  // rmsnorm_set_row_pool_shape
 std::map<std::tuple<int, int, int64_t, int, int, int, int, unsigned>, Plan> g_plans;
 std::map<std::pair<const void*, int>, bool> g_attr_done;
@@ -318,17 +319,30 @@ bool plan_tma(int pass, int64_t M, int N, int dt, int offset, int dev, const Dev
     int64_t units = 0;
     if (!occupancy_units(k, p, di, bps, units)) return false;
     p.units = units < M ? units : M;
-    // the RMSNorm backward without clusters hands the last rows of its grid out
-    // from the row pool (pool.h), when the pool kernel (one producer warp more per
-    // CTA) keeps the same residency
-    if (pass == 1 && cl == 1 && g_row_pool && stages >= 2 && stages <= kPoolMaxStages &&
-        threads <= kTmaMaxThreads && vpt <= 4) {
+    // the RMSNorm forward and backward without clusters hand the last rows of
+    // their grid out from the row pool (pool.h), when the pool kernel (one
+    // producer warp more per CTA) keeps the same residency
+    // (the forward's only with many rows per SM: at bf16 4096x4096 it measured
+    // 16.3 -> 18.5 us; with many rows one CTA more per SM than the static plan,
+    // when it fits: bf16 65536x4096 166.9 -> 165.1 us at 3 CTAs, 162.3 at 4)
+    if ((pass == 1 || (pass == 0 && M > 64 * static_cast<int64_t>(di.sms))) && cl == 1 && g_row_pool &&
+        stages >= 2 && stages <= kPoolMaxStages && threads <= kTmaMaxThreads && vpt <= 4 && vec * vpt < 64) {
         Plan q = p;
         q.extra_threads = 32;
         q.pool = make_row_pool(M, p.units, g_pool_shape);
         const void* kq = q.pool.head > 0 ? kernel_for(pass, q) : nullptr;
-        int64_t uq = 0;
-        if (kq && prepare_kernel(kq, dev, di) && occupancy_units(kq, q, di, bps, uq) && uq >= p.units) p = q;
+        if (kq && prepare_kernel(kq, dev, di)) {
+            int64_t uq = 0;
+            const int more = pass == 0 && !ov.blocks_per_sm ? bps + 1 : bps;
+            if (more > bps && occupancy_units(kq, q, di, more, uq) && uq == static_cast<int64_t>(more) * di.sms &&
+                uq < M) {
+                q.units = uq;
+                q.pool = make_row_pool(M, uq, g_pool_shape);
+                if (q.pool.head > 0) p = q;
+            } else if (occupancy_units(kq, q, di, bps, uq) && uq >= p.units) {
+                p = q;
+            }
+        }
         (void)cudaGetLastError();
     }
     return true;
@@ -714,6 +728,13 @@ rmsnorm_status fwd_impl(const void* x, int64_t ldx, const void* gamma, void* y, 
     a.eps = eps;
     a.stages = c.plan.stages;
     a.err = c.err;
+    a.pool = c.plan.pool;
+    if (a.pool.head > 0) {
+        a.queue = fwd_queue_word(g_fwd_slot.fetch_add(1u));
+        if (!a.queue) return RMSNORM_ERR_CUDA;
+        a.ticket = next_call_ticket();
+        a.pool_solo = g_row_pool == 2;
+    }
     if (launch_pass(0, c, a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
@@ -1103,9 +1124,9 @@ extern "C" rmsnorm_status rmsnorm_describe_plan(int pass, int64_t M, int64_t N, 
 }
 
 extern "C" rmsnorm_status rmsnorm_set_row_pool(int enabled) {
-    if (enabled != 0 && enabled != 1) return RMSNORM_ERR_ARG;
+    if (enabled < 0 || enabled > 2) return RMSNORM_ERR_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
-    g_row_pool = enabled != 0;
+    g_row_pool = enabled;
     ++g_override_gen;
     return RMSNORM_OK;
 }

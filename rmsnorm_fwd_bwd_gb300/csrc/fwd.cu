@@ -225,6 +225,217 @@ __global__ void __launch_bounds__(kTmaMaxThreads, (FwdTmaMinBlocks<DT, VPT>::val
     }
 }
 
+// The forward's queue words: one per call slot, in the library's own device
+// memory (the forward has no workspace). A call's CTA 0 opens its slot by storing
+// {ticket, 0}; a take whose fetch-and-add finds another ticket there (another call
+// given the same slot and running at the same time, or a take that came before
+// CTA 0's store) cannot trust the count, and that CTA then runs every segment of
+// the queue itself: rows written twice get the same values, so the result stays
+// right, only slower. Cleared at load; read and written only by forward pool
+// kernels.
+__device__ unsigned long long g_fwd_queue[kFwdQueueSlots];
+
+// Forward row kernel with the row pool of pool.h (no clusters), formulas as in
+// fwd_tma_kernel. CTA b takes rows b + j * G, j < a.pool.head, then segments of
+// consecutive rows from the call's queue word. a.threads consumer threads plus one
+// producer warp: the producer's lane 0 runs the TMA ring ahead of the consumers
+// (`full` barriers for the copies, `empty` barriers, one arrival per consumer
+// warp, before a stage is refilled), decides each stage's row and records it in
+// shared memory; a stage with no row (queue empty) ends both loops. The
+// consumers sync only on a named barrier (the row's sum of squares).
+// a.pool_solo (tuning) makes every CTA run every segment.
+template <int DT, int VPT, bool OFFSET>
+__global__ void __launch_bounds__(kTmaMaxThreads + 32) fwd_pool_kernel(const RowArgs a) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int64_t stage_row[kPoolMaxStages];
+    __shared__ uint64_t empty[kPoolMaxStages];
+
+    const int tid = threadIdx.x;
+    const int nc = blockDim.x - 32;  // consumer threads
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int ncw = nc >> 5;
+    const int64_t G = gridDim.x;
+    const int nvec = a.N / VEC;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * E::kBytes;
+    const int S = a.stages;
+
+    // shared memory: ring | full barriers | warp partials [2][32] | abort flag
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * row_bytes);
+    float* red = reinterpret_cast<float*>(full + S);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), static_cast<uint32_t>(ncw));
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+
+    if (warp == ncw) {
+        // ---------------- producer ----------------
+        if (lane != 0) return;
+        const uint32_t ticket = static_cast<uint32_t>(a.ticket);
+        const uint64_t pol = l2_evict_first_policy();
+        const char* xb = static_cast<const char*>(a.x);
+        const size_t x_pitch = static_cast<size_t>(a.ldx) * E::kBytes;
+        int64_t heads = 0, seg_row = 0, seg_end = 0, seg_id = -1;
+        bool solo = a.pool_solo != 0, done = false;
+        unsigned long long pend = 0;
+        bool pend_on = false;
+        auto take_ahead = [&]() {
+            if (!pend_on && !solo) {
+                pend = atomicAdd(a.queue, 1ull);
+                pend_on = true;
+            }
+        };
+        int64_t issued = 0;
+        bool aborted = false;
+        for (;; ++issued) {
+            const int s = static_cast<int>(issued % S);
+            const int64_t round = issued / S;
+            if (round > 0) {
+                bool ok = false;
+#pragma unroll 1
+                for (uint32_t i = 0; i < kWaitPollLimit && !ok; ++i) {
+                    ok = mbar_try_wait(smem_u32(&empty[s]), static_cast<uint32_t>((round - 1) & 1));
+                    if (!ok && *abort_flag) break;
+                }
+                if (!ok) {
+                    if (!*abort_flag) atomicOr(a.err, kDevErrWaitTimeout);
+                    aborted = true;
+                    break;
+                }
+            }
+            int64_t row = -1;
+            if (heads < a.pool.head) {
+                row = static_cast<int64_t>(blockIdx.x) + heads * G;
+                ++heads;
+                if (a.pool.head - heads <= kPoolTakeAhead) take_ahead();
+            } else if (!done) {
+                if (seg_row >= seg_end) {
+                    int64_t k;
+                    if (solo) {
+                        k = seg_id + 1;
+                    } else {
+                        take_ahead();
+                        pend_on = false;
+                        if ((pend >> 32) == ticket) {
+                            k = static_cast<int64_t>(pend & 0xffffffffull);
+                        } else {
+                            solo = true;  // the count is not this call's: run every segment
+                            k = 0;
+                        }
+                    }
+                    if (k < a.pool.nseg) {
+                        pool_segment(a.pool, k, seg_row, seg_end);
+                        seg_id = k;
+                    } else {
+                        done = true;
+                    }
+                }
+                if (!done) {
+                    row = seg_row++;
+                    if (seg_end - seg_row <= kPoolTakeAhead) take_ahead();
+                }
+            }
+            stage_row[s] = row;
+            const uint32_t bar = smem_u32(&full[s]);
+            if (row < 0) {
+                mbar_arrive(bar);
+                break;
+            }
+            mbar_arrive_expect_tx(bar, row_bytes);
+            bulk_g2s_in(smem_u32(ring + static_cast<size_t>(s) * row_bytes), xb + static_cast<size_t>(row) * x_pitch,
+                        row_bytes, bar, pol, a.x, a.M, a.ldx, a.N, E::kBytes, a.err);
+            if (issued == 0 && blockIdx.x == 0) atomicExch(a.queue, static_cast<unsigned long long>(ticket) << 32);
+        }
+        if (aborted) {
+            for (int64_t i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
+                if (stage_row[i % S] >= 0)
+                    mbar_wait_bounded(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), a.err,
+                                      1u << 16);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    float gf[VPT][VEC];
+    {
+        const uint4* gs = reinterpret_cast<const uint4*>(a.gamma);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nc + tid;
+            const uint4 raw = idx < nvec ? __ldg(gs + idx) : make_uint4(0, 0, 0, 0);
+            E::unpack(raw, gf[v]);
+            if (OFFSET) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) gf[v][e] = 1.0f + gf[v][e];
+            }
+        }
+    }
+    char* yb = static_cast<char*>(a.y);
+    const size_t y_pitch = static_cast<size_t>(a.ldy) * E::kBytes;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t j = 0;; ++j) {
+        if (!mbar_wait_bounded(smem_u32(&full[s]), parity, a.err)) *abort_flag = 1;
+        const int64_t row = stage_row[s];
+        if (row < 0) break;  // the queue is empty (every consumer reads the same stage)
+        const unsigned char* st = ring + static_cast<size_t>(s) * row_bytes;
+        float xf[VPT][VEC];
+        uint64_t ss = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nc + tid;
+            const uint4 raw = idx < nvec ? *reinterpret_cast<const uint4*>(st + idx * 16) : make_uint4(0, 0, 0, 0);
+            E::unpack(raw, xf[v]);
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                const uint64_t x2 = f2_pack(xf[v][e], xf[v][e + 1]);
+                ss = f2_fma(x2, x2, ss);
+            }
+        }
+        // this warp is done with the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        float ss0, ss1;
+        f2_unpack(ss, ss0, ss1);
+        float* redb = red + (j & 1) * 32;
+        const float wsum = warp_allsum(ss0 + ss1);
+        if (lane == 0) redb[warp] = wsum;
+        named_barrier_sync(1, nc);
+        if (*abort_flag) break;  // every consumer reads the flag after the same barrier
+        float t = lane < ncw ? redb[lane] : 0.f;
+        t = warp_allsum(t);
+        const float ms = t / static_cast<float>(a.N);
+        const float r = 1.0f / sqrtf(ms + a.eps);
+        if (tid == 0) a.rstd_out[row] = r;
+        char* yrow = yb + static_cast<size_t>(row) * y_pitch;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = v * nc + tid;
+            if (idx < nvec) {
+                float o[VEC];
+                scale_pairs<VEC, OFFSET>(xf[v], gf[v], false, r, o);
+                stg128(yrow + idx * 16, E::pack(o));
+            }
+        }
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+    griddep_launch_dependents();
+}
+
 template <int DT, bool OFFSET>
 __global__ void __launch_bounds__(kScalarThreads) fwd_scalar_kernel(const RowArgs a) {
     using E = Elem<DT>;
@@ -291,7 +502,17 @@ static const void* fwd_tma_vpt(int vpt) {
     }
 }
 template <int DT, bool OFF>
-static const void* fwd_tma_for(int vpt, int cluster) {
+static const void* fwd_pool_vpt(int vpt) {
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&fwd_pool_kernel<DT, 1, OFF>);
+    case 2: return reinterpret_cast<const void*>(&fwd_pool_kernel<DT, 2, OFF>);
+    case 4: return reinterpret_cast<const void*>(&fwd_pool_kernel<DT, 4, OFF>);
+    default: return nullptr;
+    }
+}
+template <int DT, bool OFF>
+static const void* fwd_tma_for(int vpt, int cluster, bool pool) {
+    if (pool) return fwd_pool_vpt<DT, OFF>(vpt);
     return cluster > 1 ? fwd_tma_vpt<DT, OFF, true>(vpt) : fwd_tma_vpt<DT, OFF, false>(vpt);
 }
 template <int DT, bool OFF>
@@ -301,12 +522,22 @@ static const void* fwd_scalar_for() {
 template <bool OFF>
 static const void* fwd_pick(const Plan& p) {
     const bool tma = p.path == kPathTma;
+    const bool pool = p.pool.head > 0 && p.cluster == 1;
     switch (p.dtype) {
-    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF32, OFF>();
-    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kF16, OFF>();
-    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster) : fwd_scalar_for<kBF16, OFF>();
+    case kF32: return tma ? fwd_tma_for<kF32, OFF>(p.per_thread, p.cluster, pool) : fwd_scalar_for<kF32, OFF>();
+    case kF16: return tma ? fwd_tma_for<kF16, OFF>(p.per_thread, p.cluster, pool) : fwd_scalar_for<kF16, OFF>();
+    case kBF16: return tma ? fwd_tma_for<kBF16, OFF>(p.per_thread, p.cluster, pool) : fwd_scalar_for<kBF16, OFF>();
     default: return nullptr;
     }
+}
+
+unsigned long long* fwd_queue_word(unsigned slot) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_queue) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return static_cast<unsigned long long*>(p) + slot % kFwdQueueSlots;
 }
 
 const void* fwd_kernel(const Plan& p) {

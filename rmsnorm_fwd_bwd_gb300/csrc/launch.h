@@ -40,6 +40,7 @@ struct RowArgs {
                                 // {call ticket (high 32 bits), segments taken}
     unsigned long long ticket;  // this call's ticket (low 32 bits used; consecutive
                                 // calls in a process never share one)
+    int pool_solo;              // forward pool, tuning: every CTA runs every segment
 };
 
 enum PathKind : int { kPathTma = 0, kPathScalar = 1, kPathRowVec = 2, kPathRagged = 3, kPathLanes = 4 };
@@ -76,6 +77,8 @@ constexpr int kScalarThreads = 256;
 // (the take's round trip then overlaps those rows).
 constexpr int kPoolMaxStages = 8;
 constexpr int kPoolTakeAhead = 2;
+// Queue words of the forward's row pool, one per call slot (fwd.cu).
+constexpr unsigned kFwdQueueSlots = 4096;
 
 // A launch shape chosen by the planner.
 struct Plan {
@@ -132,5 +135,8 @@ cudaError_t launch_dgamma_reduce(int dtype, const float* ws, int64_t units, int 
 // Device address of the error word in the current context (nullptr on failure),
 // looked up on every call.
 uint32_t* device_error_word();
+// Device address of the forward pool's queue word for a call slot (nullptr on
+// failure), looked up on every call.
+unsigned long long* fwd_queue_word(unsigned slot);
 
 }  // namespace rmsnorm

@@ -26,9 +26,11 @@ rmsnorm_status rmsnorm_set_launch_override(int pass, int threads, int vpt, int s
                                            int blocks_per_sm);
 
 /*
- * Turn the RMSNorm backward's row pool on (1, the default) or off (0: every CTA
- * takes the rows b, b + G, ... of the static assignment). Process-wide, like the
- * override above; for comparing the two assignments.
+ * Turn the RMSNorm forward's and backward's row pool on (1, the default) or off
+ * (0: every CTA takes the rows b, b + G, ... of the static assignment); 2 keeps
+ * it on but makes every CTA of a forward run every queued segment (the path a
+ * forward takes when its queue word is not its own). Process-wide, like the
+ * override above; for comparing the assignments.
  */
 rmsnorm_status rmsnorm_set_row_pool(int enabled);
 

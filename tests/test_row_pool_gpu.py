@@ -143,9 +143,10 @@ def test_small_workspace_takes_the_static_assignment():
 
 
 def test_pool_backward_replayed_from_a_cuda_graph():
-    """A captured forward + backward repeats the same call ticket on every replay;
-    the column reduce closes the queue word after each call, so every replay (with
-    new inputs copied into the captured buffers) gives the eager bits."""
+    """A captured forward + backward repeats the same call tickets on every replay;
+    the forward's CTA 0 reopens its queue word and the backward's column reduce
+    closes its own after each call, so every replay (with new inputs copied into
+    the captured buffers) gives the eager bits."""
     torch = pytest.importorskip("torch")
     from rmsnorm_fwd_bwd_gb300 import binding as B
     M, N, dtype = BASE
@@ -173,7 +174,7 @@ def test_pool_backward_replayed_from_a_cuda_graph():
         load(k)
         step()
         torch.cuda.synchronize()
-        refs.append((dx.clone(), dg.clone()))
+        refs.append((dx.clone(), dg.clone(), y.clone(), r.clone()))
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -183,9 +184,39 @@ def test_pool_backward_replayed_from_a_cuda_graph():
     with torch.cuda.graph(graph):
         step()
     for _ in range(2):
-        for k, (rdx, rdg) in enumerate(refs):
+        for k, (rdx, rdg, ry, rr) in enumerate(refs):
             load(k)
             graph.replay()
             torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int16), ry.view(torch.int16)), f"y differs on replay {k}"
+            assert torch.equal(r, rr), f"rstd differs on replay {k}"
             assert torch.equal(dx.view(torch.int16), rdx.view(torch.int16)), f"dx differs on replay {k}"
             assert torch.equal(dg.view(torch.int16), rdg.view(torch.int16)), f"dgamma differs on replay {k}"
+
+
+@pytest.mark.parametrize("M,N,dtype,offset", [(10000, 4096, "bfloat16", False), (12000, 2048, "float16", True),
+                                              (10000, 2048, "float32", False), (4096, 4096, "bfloat16", True)])
+def test_forward_pool_matches_static_and_every_cta_running_every_segment(M, N, dtype, offset):
+    """y and r of a row do not depend on which CTA computed it: the forward pool,
+    the static assignment, and the pool with its queue bypassed (every CTA runs
+    every queued segment, the path of a forward whose queue word is not its own)
+    give the same bits; the pool's result is gated against the oracle."""
+    from rmsnorm_fwd_bwd_gb300 import binding as B
+    plan = B.rmsnorm_describe_plan(0, M, N, dtype)
+    if "pool_head=" not in plan:
+        pytest.skip(f"no row pool in this plan: {plan}")
+    x, g, dy = inputs.make_inputs(M, N, dtype, seed=M + 3 * N, offset=offset)
+    outs = {}
+    try:
+        for mode in (1, 0, 2):
+            assert B.rmsnorm_set_row_pool(mode) == 0
+            y, r, _, _ = gpu_util.run(x, g, dy, dtype, offset=offset, do_bwd=False)
+            outs[mode] = (y, r)
+    finally:
+        assert B.rmsnorm_set_row_pool(1) == 0
+    for mode in (0, 2):
+        assert np.array_equal(outs[mode][0], outs[1][0]) and np.array_equal(outs[mode][1], outs[1][1]), mode
+    res = check.gate_outputs(x, g, dy, dtype, offset, 1e-6, y=outs[1][0], rstd=outs[1][1])
+    text = gate.report(f"forward pool {plan}", res)
+    print("\n" + text)
+    assert gate.overall(res) == "PASS", text
