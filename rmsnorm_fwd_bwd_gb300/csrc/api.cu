@@ -875,8 +875,7 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     CallPlan c;
     if ((st = plan_call(3, M, static_cast<int>(N), dtype, 0, layout, c)) != RMSNORM_OK) return st;
     const Plan& p = c.plan;
-    const size_t need = 2 * static_cast<size_t>(p.units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
-    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_need(p, N, 2)) return RMSNORM_ERR_WORKSPACE;
     RowArgs a = {};
     a.x = x;
     a.gamma = gamma;
@@ -894,7 +893,8 @@ rmsnorm_status ln_bwd_impl(const void* dy, int64_t lddy, const void* x, int64_t 
     a.stages = p.stages;
     a.err = c.err;
     if (launch_pass(3, c, a, cs) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, dgamma, cs, dbeta) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (launch_dgamma_reduce(dtype, a.ws, p.units, a.N, a.ldws, dgamma, cs, dbeta) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -1021,11 +1021,12 @@ extern "C" size_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dty
     int dev = 0;
     DeviceInfo* di = nullptr;
     if (current_device(dev, di) != RMSNORM_OK) return 0;
-    int64_t units = 0;
+    size_t need = 0;
     Plan p;
     for (int layout : {kLayoutMixed, kLayoutAligned, kLayoutPhase})
-        if (get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p) && p.units > units) units = p.units;
-    return 2 * static_cast<size_t>(units) * static_cast<size_t>(workspace_pitch(N)) * sizeof(float);
+        if (get_plan(3, M, static_cast<int>(N), dtype, 0, layout, dev, *di, p))
+            need = std::max(need, workspace_need(p, N, 2));
+    return need;
 }
 
 extern "C" rmsnorm_status layernorm_bwd(const void* dy, int64_t lddy, const void* x, int64_t ldx, const void* gamma,

@@ -103,3 +103,33 @@ def test_strided_rejects_short_pitch(torch):
     g = torch.ones(64, device="cuda")
     r = torch.empty(4, device="cuda")
     assert B.rmsnorm_fwd_strided(x, 63, g, x, 64, r, 4, 64, 1e-6, "float32", 0) == 2  # SHAPE
+
+
+def test_strided_rows_with_the_row_pool(torch):
+    """Rows the row pool hands out (heads and queued segments, forward and backward)
+    use each tensor's own pitch: at 12000 rows the strided calls give the dense
+    calls' bits and never touch the gaps between rows."""
+    M, N, dtype = 12000, 4096, "bfloat16"
+    for p in (0, 1):
+        plan = B.rmsnorm_describe_plan(p, M, N, dtype)
+        assert "pool_head=" in plan, plan
+    x, g, dy = inputs.make_inputs(M, N, dtype, seed=21)
+    from tests import gpu_util
+    dense = gpu_util.run(x, g, dy, dtype)
+    ldx, lddy, ldo = 4160, 4176, 4168
+    xb, dyb = _wide(torch, x, ldx, dtype), _wide(torch, dy, lddy, dtype)
+    gt = B.to_device(g, dtype)
+    yb, dxb = _out(torch, M, N, ldo, dtype), _out(torch, M, N, ldo, dtype)
+    dg = torch.empty_like(gt)
+    rstd = torch.empty(M, dtype=torch.float32, device="cuda")
+    assert B.rmsnorm_fwd_strided(xb, ldx, gt, yb, ldo, rstd, M, N, 1e-6, dtype, 0) == 0
+    need = B.rmsnorm_bwd_workspace_size(M, N, dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert B.rmsnorm_bwd_strided(dyb, lddy, xb, ldx, gt, rstd, dxb, ldo, dg, M, N, dtype, 0, ws, need) == 0
+    torch.cuda.synchronize()
+    for buf in (yb, dxb):
+        assert torch.all(buf[:, N:] == SENT[dtype]), "a gap element between rows was written"
+    assert np.array_equal(B.to_numpy(yb[:, :N].contiguous(), dtype), dense[0])
+    assert np.array_equal(B.to_numpy(rstd, "float32"), dense[1])
+    assert np.array_equal(B.to_numpy(dxb[:, :N].contiguous(), dtype), dense[2])
+    assert np.array_equal(B.to_numpy(dg, dtype), dense[3])
