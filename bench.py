@@ -18,8 +18,12 @@ e2e    = the same metric through the C ABI with host buffers: each step copies
          step's bytes in both directions at once, timed in the same run.
 roofline = the backward pass (the dominant cost) against the measured HBM copy
          bandwidth in MEASURED_PEAKS.json.
-cpu_baseline / --impl reference = the CPU oracle (single-threaded C,
-         fp32-intermediate reference) on a bounded row sample of the workload.
+cpu_baseline / --impl reference = the CPU oracle (its C fp32-intermediate
+         reference, rows split over every core of the process's affinity mask;
+         cpu_baseline also times one thread and the fp64 golden) on a bounded
+         row sample of the workload.
+--static-rows: the RMSNorm plans without the row pool (every block keeps a fixed
+         share of the rows), for comparison.
 
 --double-backward: the step is one RMSNorm double backward (rmsnorm_bwd_bwd:
          fused row kernel + d_gamma column reduction) on the workload, with
