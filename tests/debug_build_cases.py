@@ -4,8 +4,9 @@ the extent of the tensor it reads, and a read outside it sets bit 1 of the
 device error word. Run as ``RMSNORM_LIBRARY=<debug .so> python -m
 tests.debug_build_cases``: each case is gated against the oracle and the error
 word must stay 0. Covers every path that reads with TMA copies: the aligned ring
-(one CTA and clusters), the ragged ring at shifted pointers and odd pitches,
-LayerNorm and the double backward, plus the lane-group and row-vector paths.
+(one CTA and clusters), the row pool's kernels, the ragged ring at shifted pointers
+and odd pitches, LayerNorm and the double backward, plus the lane-group and
+row-vector paths.
 """
 import sys
 
@@ -24,10 +25,13 @@ def main() -> int:
     B.rmsnorm_device_error(clear=True)
     results = []
     # RMSNorm: aligned ring, clusters, ragged (dense, shifted), row-vector, lanes
+    # (and the row pool's forward and backward, 10001 rows: heads, then queued
+    # segments, the last one short)
     for M, N, dt, off, mis in ((67, 4096, "bfloat16", False, False), (9, 16384, "float32", True, False),
                                (37, 4099, "bfloat16", False, False), (29, 4099, "float32", True, False),
                                (33, 4096, "bfloat16", False, True), (41, 2051, "float16", False, True),
-                               (13, 9999, "bfloat16", False, False), (257, 256, "bfloat16", False, False)):
+                               (13, 9999, "bfloat16", False, False), (257, 256, "bfloat16", False, False),
+                               (10001, 4096, "bfloat16", True, False)):
         x, g, dy = inputs.make_inputs(M, N, dt, seed=M + N, offset=off)
         y, r, dx, dg = gpu_util.run(x, g, dy, dt, offset=off, misalign={"x", "dy"} if mis else False)
         results += check.gate_outputs(x, g, dy, dt, off, 1e-6, y=y, rstd=r, dx=dx, dgamma=dg)
