@@ -9,13 +9,15 @@
 //
 // The row pass is one fused kernel: x and dy are read once (TMA ring as in the
 // forward), dx is written, and each persistent block keeps fp32 dgamma
-// accumulators for its fixed columns in registers across all of its rows. At the
-// end each block (cluster) writes one row of partials to the workspace. A second
-// kernel sums the partial rows per column in a fixed order, so dgamma is
-// deterministic and no floating-point atomics are used (the page's own reason
-// for private partial rows followed by a column pass). The workspace is
-// units x N floats, units ~ 2-3 x #SMs, instead of one row of partials per
-// input row.
+// accumulators for its fixed columns in registers across its rows. In
+// bwd_tma_kernel every block (cluster) takes a fixed share of the rows and writes
+// one row of partials at the end; bwd_pool_kernel (the row pool of pool.h) takes a
+// fixed head of rows, then segments of rows from a queue, and writes one partial
+// row per head and per segment. A second kernel sums the partial rows per column
+// in a fixed order, so dgamma is deterministic and no floating-point atomics are
+// used (the page's own reason for private partial rows followed by a column
+// pass). The workspace is a few rows per SM of N floats instead of one row of
+// partials per input row.
 #include "device.cuh"
 #include "launch.h"
 #include "pool.cuh"

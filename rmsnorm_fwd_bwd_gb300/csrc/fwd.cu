@@ -8,7 +8,7 @@
 // taken over the logical N, never over a padded width ("N and BLOCK: two sizes
 // you must never confuse").
 //
-// Two kernels:
+// Kernels:
 //  * fwd_tma_kernel: persistent; each cluster of C CTAs owns rows cid, cid+K, ...
 //    and CTA c of the cluster owns the column slice [c*N/C, (c+1)*N/C). A ring
 //    of `stages` shared-memory buffers is filled by TMA bulk copies
@@ -18,6 +18,9 @@
 //    memory) with one barrier per row; every CTA then forms the same total in the
 //    same order. Output vectors go straight from registers to HBM with 16-byte
 //    coalesced stores.
+//  * fwd_pool_kernel: the same ring without clusters, with the row pool of
+//    pool.h (a fixed head of rows per CTA, then segments of rows from a queue)
+//    and a producer warp per CTA that keeps the ring full;
 //  * fwd_scalar_kernel: any N and any element alignment; one CTA per row,
 //    element-strided scalar loads that stay coalesced across a warp, two passes
 //    over the row (the second one is served by L1/L2), few registers so that
