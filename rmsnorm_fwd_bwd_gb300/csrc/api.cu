@@ -141,9 +141,14 @@ uint32_t* error_word_address() {
 // again).
 unsigned long long next_call_ticket() {
     static std::atomic<uint32_t> counter{[] {
-        std::random_device rd;
         const auto t = std::chrono::steady_clock::now().time_since_epoch().count();
-        return static_cast<uint32_t>(rd()) ^ static_cast<uint32_t>(t) ^ static_cast<uint32_t>(t >> 32);
+        uint32_t seed = static_cast<uint32_t>(t) ^ static_cast<uint32_t>(t >> 32);
+        try {
+            std::random_device rd;  // may throw where the platform has no entropy source
+            seed ^= static_cast<uint32_t>(rd());
+        } catch (...) {
+        }
+        return seed;
     }()};
     return counter.fetch_add(1u);
 }
