@@ -66,3 +66,15 @@ def test_bad_arguments():
         B.rmsnorm_row_pool_segment(65536, 456, 10 ** 6)
     with pytest.raises(B.RMSNormError):
         B.rmsnorm_row_pool_segment(65536, 456, -1)
+
+
+def test_tuning_switches_validate_their_arguments():
+    """rmsnorm_set_row_pool takes 0, 1 or 2; rmsnorm_set_row_pool_shape takes head
+    shares below 100% and non-negative lengths (0: the default). Host-only: they
+    set the next plans and launch nothing."""
+    assert B.rmsnorm_set_row_pool(3) == 9       # RMSNORM_ERR_ARG
+    assert B.rmsnorm_set_row_pool(-1) == 9
+    assert B.rmsnorm_set_row_pool_shape(100, 0, 0, 0) == 9
+    assert B.rmsnorm_set_row_pool_shape(0, 0, -1, 0) == 9
+    assert B.rmsnorm_set_row_pool(1) == 0
+    assert B.rmsnorm_set_row_pool_shape(0, 0, 0, 0) == 0
